@@ -1,0 +1,118 @@
+/*
+ * Seeded synthetic inputs for the MoGE layer (input generation only).
+ *
+ * This file holds no arithmetic of the layer itself: it only draws numbers.
+ * Both the CPU oracle and the CUDA path consume the arrays it writes, so the
+ * two sides always see identical inputs.
+ *
+ * Generator (counter based, so the output does not depend on thread count):
+ *   key(seed, tensor) = splitmix64(seed XOR tensor_id)
+ *   word(i)           = splitmix64(key + i)
+ * splitmix64 is the 64-bit mixer of Steele, Lea and Flood ("Fast splittable
+ * pseudorandom number generators", OOPSLA 2014), written here from that
+ * definition: add the golden-ratio increment, then two xor-shift-multiply
+ * rounds and a final xor-shift.
+ *
+ * Normal draws use the Box-Muller transform (Box and Muller, 1958) on the pair
+ * of words (2j, 2j+1): u1 in (0,1], u2 in [0,1), r = sqrt(-2 ln u1); element
+ * 2j takes r*cos(2 pi u2) and element 2j+1 takes r*sin(2 pi u2). All of it in
+ * double, then scaled by the requested standard deviation and rounded once to
+ * fp32. bf16 values are the fp32 values rounded to nearest-even.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static inline uint64_t mix64(uint64_t z) {
+    z += 0x9E3779B97F4A7C15ULL;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+static inline uint64_t stream_key(uint64_t seed, uint64_t tensor_id) {
+    return mix64(seed ^ tensor_id);
+}
+
+/* Both normals of pair j. */
+static inline void normal_pair(uint64_t key, uint64_t j, double *z0, double *z1) {
+    uint64_t w1 = mix64(key + 2 * j);
+    uint64_t w2 = mix64(key + 2 * j + 1);
+    double u1 = (double)((w1 >> 11) + 1) * 0x1p-53; /* (0, 1] */
+    double u2 = (double)(w2 >> 11) * 0x1p-53;       /* [0, 1) */
+    double r = sqrt(-2.0 * log(u1));
+    double a = 6.283185307179586476925286766559 * u2;
+    *z0 = r * cos(a);
+    *z1 = r * sin(a);
+}
+
+static inline uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    u += 0x7FFFu + ((u >> 16) & 1u); /* finite inputs only */
+    return (uint16_t)(u >> 16);
+}
+
+/* Elements [start, start+count) of the stream, as fp32 (std * N(0,1)). */
+void synth_normal_f32(uint64_t seed, uint64_t tensor_id, uint64_t start, uint64_t count,
+                      double stddev, float *out) {
+    const uint64_t key = stream_key(seed, tensor_id);
+    const int64_t n = (int64_t)count;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        uint64_t g = start + (uint64_t)i;
+        double z0, z1;
+        normal_pair(key, g >> 1, &z0, &z1);
+        out[i] = (float)(stddev * ((g & 1) ? z1 : z0));
+    }
+}
+
+/* Same stream, rounded on to bf16 (stored as raw uint16 bits). */
+void synth_normal_bf16(uint64_t seed, uint64_t tensor_id, uint64_t start, uint64_t count,
+                       double stddev, uint16_t *out) {
+    const uint64_t key = stream_key(seed, tensor_id);
+    const int64_t n = (int64_t)count;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        uint64_t g = start + (uint64_t)i;
+        double z0, z1;
+        normal_pair(key, g >> 1, &z0, &z1);
+        out[i] = f32_to_bf16_rne((float)(stddev * ((g & 1) ? z1 : z0)));
+    }
+}
+
+/* fp32 -> bf16 (nearest-even) for an existing array. */
+void synth_f32_to_bf16(const float *in, uint64_t count, uint16_t *out) {
+    const int64_t n = (int64_t)count;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bf16_rne(in[i]);
+}
+
+/* Seeded permutation of 1..n (Fisher-Yates, descending i, j = word(i) mod (i+1)). */
+void synth_rank_permutation(uint64_t seed, uint64_t tensor_id, int64_t n, int32_t *rank) {
+    const uint64_t key = stream_key(seed, tensor_id);
+    for (int64_t i = 0; i < n; ++i) rank[i] = (int32_t)(i + 1);
+    for (int64_t i = n - 1; i > 0; --i) {
+        int64_t j = (int64_t)(mix64(key + (uint64_t)i) % (uint64_t)(i + 1));
+        int32_t t = rank[i];
+        rank[i] = rank[j];
+        rank[j] = t;
+    }
+}
+
+/* Popularity skew of the router: b_e = scale * ln(1 / rank_e), rounded to fp32. */
+void synth_rank_bias(const int32_t *rank, int64_t n, double scale, float *bias) {
+    for (int64_t i = 0; i < n; ++i) bias[i] = (float)(scale * log(1.0 / (double)rank[i]));
+}
+
+int synth_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
