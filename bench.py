@@ -1,0 +1,445 @@
+"""Benchmark of the MoGE layer forward on B300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one whole layer forward (routing, permutation, gather, grouped
+gate/up GEMM with SwiGLU, grouped down GEMM, combine, imbalance score) over one
+batch of seeded synthetic tokens, through the C ABI (moge_layer_forward).  The
+headline workload is the prefill layer (T=8192, d=4096, N=64 in 8 groups,
+K'=2, I=1408, bf16 with fp32 accumulation); the decode layer (T=32, same
+weights) is measured in the same run and reported under "decode".
+
+Under torchrun (N>1) every rank runs an independent replica of the layer on
+its own GPU (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import WORKLOADS, DEFAULT_SEED  # noqa: E402
+
+METRIC = "MoGE layer tokens/s (decode T=32, prefill T=8192); % of HBM / bf16 TC roofline"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+KERNEL_SRC = os.path.join(ROOT, "sparse_router_gemm_global_b300", "csrc", "ffn_tc.cu")
+
+
+# --------------------------------------------------------------------------------------------
+# environment helpers
+# --------------------------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    if os.path.exists(PEAKS_PATH):
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(key: str):
+    """DRAM bytes per launch from an ncu capture, if taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_PATH):
+        return None
+    with open(TRAFFIC_PATH) as f:
+        rec = json.load(f)
+    ent = rec.get(key)
+    if not ent or ent.get("kernel_sha256_16") != kernel_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moge_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------------------------
+
+def upload(inp, device):
+    import torch
+    out = {}
+    for k, v in inp.items():
+        v = np.ascontiguousarray(v)
+        if v.dtype == np.uint16:
+            out[k] = torch.from_numpy(v.view(np.int16)).to(device).view(torch.bfloat16)
+        else:
+            out[k] = torch.from_numpy(v).to(device)
+    return out
+
+
+class Layer:
+    """Device buffers of one workload and the C-ABI call of one step."""
+
+    def __init__(self, w, d_inp, device):
+        import torch
+        import sparse_router_gemm_global_b300 as moge
+        self.moge, self.w, self.dev = moge, w, device
+        self.cfg = moge.make_config(w.T, w.d, w.N, w.M, w.kpg, w.I, w.dtype)
+        self.ws = moge.alloc_workspace(self.cfg, device)
+        self.d = d_inp
+        self.x = d_inp["x"][: w.T].contiguous()
+        self.y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=device)
+        self.aux = {"counts": torch.empty(w.N, dtype=torch.int32, device=device),
+                    "group_load": torch.empty(w.M, dtype=torch.int32, device=device),
+                    "score": torch.empty(4, dtype=torch.float32, device=device)}
+
+    def step(self, x=None, y=None):
+        d = self.d
+        self.moge.moge_layer_forward(self.cfg, self.x if x is None else x, d["w_router"], d["bias"], d["w_gate"],
+                                     d["w_up"], d["w_down"], self.y if y is None else y, self.ws, aux=self.aux)
+
+
+def timed_steps(layer, steps, warmup, dist, stage_events=True):
+    """K steps bracketed by barrier + synchronize; returns (ms/step max over ranks, stage ms means)."""
+    import torch
+    moge = layer.moge
+    for _ in range(warmup):
+        layer.step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moge.MOGE_NUM_STAGES + 1)]
+           for _ in range(steps)] if stage_events else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n0 = moge.moge_kernel_launch_count()
+    start.record()
+    for i in range(steps):
+        if evs is not None:
+            moge.moge_set_stage_events(evs[i])
+        layer.step()
+    end.record()
+    torch.cuda.synchronize()
+    if evs is not None:
+        moge.moge_set_stage_events(None)
+    launches = moge.moge_kernel_launch_count() - n0
+    if dist:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(end) / steps
+    if dist:
+        t = torch.tensor([ms], device=layer.dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    stages = None
+    if evs is not None:
+        stages = {}
+        for s, name in enumerate(moge.STAGE_NAMES):
+            stages[name] = statistics.fmean(e[s].elapsed_time(e[s + 1]) for e in evs)
+    if moge.moge_query_device_status(layer.ws) != 0:
+        raise RuntimeError("device status reports a timed-out wait")
+    return ms, stages, launches
+
+
+def e2e_steps(layer, steps, dist):
+    """Same metric through the public call with host buffers: pinned H2D of x and D2H of y per step."""
+    import torch
+    w = layer.w
+    x_host = layer.x.cpu().pin_memory()
+    y_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(layer.x)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.step(x=x_dev)
+        y_host.copy_(layer.y, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.step(x=x_dev)
+        y_host.copy_(layer.y, non_blocking=True)
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    if dist:
+        t = torch.tensor([ms], device=layer.dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, x_host.numel() * 2, y_host.numel() * 2
+
+
+def gate_up_roofline(w, counts, stage_ms, pk, peak_kind):
+    """Roofline of the dominant kernel (grouped gate/up GEMM + SwiGLU) from its stage time."""
+    P = w.P
+    touched = int((counts > 0).sum())
+    flops = 4.0 * P * w.d * w.I
+    bytes_alg = touched * 2 * w.I * w.d * 2 + P * w.d * 2 + P * w.I * 2
+    sec = stage_ms / 1e3
+    if w.T >= 1024:  # tensor-core bound shape
+        achieved = flops / sec / 1e12
+        peak = pk["bf16_tflops"]
+        rl = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+              "frac": round(achieved / peak, 4), "peak_kind": f"bf16 burst, {peak_kind}",
+              "algorithmic_per_launch": {"flop": flops}, "kernel": "gate_up grouped GEMM + SwiGLU"}
+    else:
+        achieved = bytes_alg / sec / 1e9
+        peak = pk["hbm_gbs"]
+        rl = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+              "frac": round(achieved / peak, 4), "peak_kind": f"HBM copy, {peak_kind}",
+              "algorithmic_per_launch": {"bytes": bytes_alg, "touched_experts": touched},
+              "kernel": "gate_up grouped GEMM + SwiGLU"}
+    rl["traffic"] = recorded_traffic(w.name + ":gate_up")
+    rl["launch_ms"] = round(stage_ms, 5)
+    return rl
+
+
+def layer_roofline(w, counts, ms, pk):
+    """Whole-layer fractions for context: FLOP vs TC peak and touched weight bytes vs HBM peak."""
+    touched = int((counts > 0).sum())
+    flops = 6.0 * w.P * w.d * w.I + 2.0 * w.T * w.d * w.N
+    wbytes = touched * 3 * w.I * w.d * 2
+    sec = ms / 1e3
+    return {"tflops": round(flops / sec / 1e12, 2), "tc_frac": round(flops / sec / 1e12 / pk["bf16_tflops"], 4),
+            "weight_gbs": round(wbytes / sec / 1e9, 1), "hbm_frac": round(wbytes / sec / 1e9 / pk["hbm_gbs"], 4),
+            "touched_experts": touched}
+
+
+def cpu_baseline(w, inp, budget_s=10.0):
+    """The oracle as it stands, on this host's cores: routing of every token plus the
+    expert FFN + combine of a token sample sized to ~budget_s; tokens/s extrapolated."""
+    import oracle
+    cores = oracle.num_threads()
+    t0 = time.perf_counter()
+    logits = oracle.router_logits(inp["x"], inp["w_router"], inp["bias"])
+    r = oracle.route(logits, w.M, w.kpg)
+    t_route = time.perf_counter() - t0
+    probe = np.arange(min(4, w.T), dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.combine_tokens(probe, r["idx"], r["gate64"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
+    per_tok = (time.perf_counter() - t0) / len(probe)
+    n = int(max(len(probe), min(w.T, budget_s / max(per_tok, 1e-9))))
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(w.T, n, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.combine_tokens(sample, r["idx"], r["gate64"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
+    t_ffn = time.perf_counter() - t0
+    sec_per_token = t_route / w.T + t_ffn / n
+    return {"value": round(1.0 / sec_per_token, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{w.name}: routing of all {w.T} tokens ({t_route:.2f} s) + expert FFN and combine of "
+                      f"{n} sampled tokens ({t_ffn:.2f} s), per-token cost extrapolated to T={w.T}"}
+
+
+def run_ours(args):
+    import torch
+    ws_n, rank, local = dist_env()
+    dist = ws_n > 1
+    if dist:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pk, peak_kind = peaks()
+
+    wp = WORKLOADS[args.workload]
+    wd = WORKLOADS["decode_t32"]
+    inp = synth.layer_inputs(wp, seed=DEFAULT_SEED)   # decode reuses the same weights and the first 32 tokens
+    d_inp = upload(inp, device)
+
+    prefill = Layer(wp, d_inp, device)
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if dist else \
+        os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+    gpu_index = int(phys) if phys.isdigit() else local
+    with ClockSampler(gpu_index) as clk:
+        ms, stages, launches = timed_steps(prefill, args.steps, args.warmup, dist)
+    clocks = clk.summary()
+    counts = prefill.aux["counts"].cpu().numpy()
+    score = float(prefill.aux["score"][0].item())
+
+    # decode shape, same weights
+    dec = Layer(wd, d_inp, device)
+    dms, dstages, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist)
+    dcounts = dec.aux["counts"].cpu().numpy()
+
+    # end to end through the public call with host buffers
+    e2e_ms, h2d, d2h = e2e_steps(prefill, max(3, args.steps // 2), dist)
+
+    tok = wp.T * ws_n
+    res = {
+        "metric": METRIC,
+        "value": round(tok / (ms / 1e3), 1),
+        "unit": "tokens/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded splitmix64 + Box-Muller; random-init weights N(0,1/fan_in), "
+                "router bias 1.5 ln(1/rank_e))",
+        "config": {"workload": wp.name, "T": wp.T, "d": wp.d, "N": wp.N, "M": wp.M, "k_per_group": wp.kpg,
+                   "K": wp.K, "I": wp.I, "seed": DEFAULT_SEED, "parallelism": f"replicas x{ws_n}",
+                   "l2": "inputs larger than L2 (2.2 GB of expert weights, 1 GB permuted activations)"},
+        "roofline": gate_up_roofline(wp, counts, stages["gate_up"], pk, peak_kind),
+        "layer_roofline": layer_roofline(wp, counts, ms, pk),
+        "stage_ms": {k: round(v, 5) for k, v in stages.items()},
+        "imbalance_score": score,
+        "clocks": clocks,
+        "e2e": {"value": round(tok / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": int(launches),
+        "decode": {"workload": wd.name, "value": round(wd.T * ws_n / (dms / 1e3), 1), "unit": "tokens/s",
+                   "ms_per_step": round(dms, 4), "steps": args.decode_steps,
+                   "roofline": gate_up_roofline(wd, dcounts, dstages["gate_up"], pk, peak_kind),
+                   "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
+                   "stage_ms": {k: round(v, 5) for k, v in dstages.items()}, "gpu_launches": int(dlaunches)},
+    }
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wp, inp, budget_s=args.cpu_budget)
+    if dist:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+# --------------------------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands (no reference code exists to install)
+# --------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = WORKLOADS[args.workload]
+    inp = synth.layer_inputs(w, seed=DEFAULT_SEED)
+    cores = oracle.num_threads()
+    rng = np.random.default_rng(0)
+
+    def one_step(n_sample):
+        t0 = time.perf_counter()
+        logits = oracle.router_logits(inp["x"], inp["w_router"], inp["bias"])
+        r = oracle.route(logits, w.M, w.kpg)
+        t_route = time.perf_counter() - t0
+        sample = np.sort(rng.choice(w.T, n_sample, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.combine_tokens(sample, r["idx"], r["gate64"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
+        t_ffn = time.perf_counter() - t0
+        return t_route / w.T + t_ffn / n_sample
+
+    n_sample = max(1, args.ref_tokens)
+    for _ in range(args.warmup):
+        one_step(n_sample)
+    per_tok = [one_step(n_sample) for _ in range(args.steps)]
+    sec = statistics.fmean(per_tok)
+    value = round(1.0 / sec, 3)
+    sample_desc = (f"{w.name}: each step routes all {w.T} tokens and runs the expert FFN + combine of "
+                   f"{n_sample} sampled tokens; per-token cost extrapolated to T={w.T}")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * w.T * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "M": w.M,
+                                                 "k_per_group": w.kpg, "I": w.I, "seed": DEFAULT_SEED},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample_desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--decode-steps", type=int, default=300)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_t8192", choices=["prefill_t8192"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle FFN work")
+    ap.add_argument("--ref-tokens", type=int, default=8, help="FFN tokens per reference-arm step")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

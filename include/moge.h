@@ -1,0 +1,213 @@
+/*
+ * moge.h -- C ABI of the B300 (sm_103a) Mixture-of-Grouped-Experts layer forward.
+ *
+ * The layer ("Pangu Pro MoE: Mixture of Grouped Experts for Efficient
+ * Sparsity", retold in the Pangu Pro MoE explainer, section 1 "innovative
+ * architecture"): N experts are split evenly into M groups of G = N/M; each
+ * token's router scores go through one softmax over all N experts; inside
+ * every group exactly K' = K/M experts are selected, so every group (one
+ * device in expert parallelism) receives the same load and the imbalance
+ * score is zero.  Tokens are then permuted to their experts, each selected
+ * expert runs a SwiGLU FFN as a grouped GEMM, and the expert outputs are
+ * summed weighted by their gates.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Memory: every pointer argument is DEVICE memory owned by the caller
+ *    (except `cfg`, which is host memory read during the call).  The library
+ *    allocates, frees and synchronises nothing on these paths; scratch space
+ *    is the caller's `ws` buffer of `ws_bytes` bytes, sized by
+ *    moge_workspace_bytes().
+ *  - Streams: all device work is enqueued on `stream` (0 = legacy default).
+ *    A call returns once its work is enqueued.
+ *  - Layouts (row-major, contiguous): x [T,d]; w_router [N,d];
+ *    w_gate, w_up [N,I,d]; w_down [N,d,I]; logits [T,N];
+ *    topk_idx, topk_gate, pair_row [T,K] with K = M*K'; counts [N];
+ *    offsets [N+1]; row_token [P] with P = T*K; x_perm [P,d]; y_perm [P,d];
+ *    y [T,d]; group_load [M]; score: one float.
+ *  - Element types: activations (x, x_perm, y_perm, y) and weights (w_*)
+ *    have the configuration's dtype (fp32, or bf16 as raw 16-bit values);
+ *    bias, logits, gates and score are fp32; indices and counts are int32.
+ *  - Alignment: device pointers must be 16-byte aligned (MOGE_ERR_INVALID_ARGUMENT
+ *    otherwise); the workspace must be 256-byte aligned.
+ *  - Errors: argument checks run on the host before anything is launched;
+ *    a rejected call leaves every output untouched.  Inputs must be finite
+ *    (non-finite values are a precondition violation, not detected).
+ *    Every bounded wait inside a kernel that gives up records
+ *    MOGE_ERR_TIMEOUT in the workspace status word instead of hanging; read
+ *    it with moge_query_device_status().
+ *  - Determinism: every output is bit-reproducible for identical inputs and
+ *    configuration (no floating-point atomics; fixed summation orders).
+ */
+#ifndef MOGE_H
+#define MOGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOGE_ABI_VERSION 1
+
+typedef struct CUstream_st *moge_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+    MOGE_OK = 0,
+    MOGE_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad shape, N % M != 0, K' outside [1, N/M], misalignment */
+    MOGE_ERR_UNSUPPORTED = 2,      /* dtype/shape combination this build does not handle */
+    MOGE_ERR_WORKSPACE = 3,        /* ws is NULL or ws_bytes < moge_workspace_bytes(cfg) */
+    MOGE_ERR_CUDA = 4,             /* a CUDA runtime call or kernel launch failed */
+    MOGE_ERR_TIMEOUT = 5           /* a bounded device-side wait gave up (see moge_query_device_status) */
+} moge_status_t;
+
+typedef enum { MOGE_F32 = 0, MOGE_BF16 = 1 } moge_dtype_t;
+
+typedef enum {
+    MOGE_ROUTE_GROUPED = 0,    /* MoGE: top-K' inside each of the M groups */
+    MOGE_ROUTE_GLOBAL_TOPK = 1 /* conventional MoE: top-K (K = M*K') over all N experts */
+} moge_route_mode_t;
+
+/* Layer shape.  T tokens, hidden size d, N experts in M groups, K' =
+ * k_per_group experts chosen per group, expert FFN intermediate size I.
+ * act_dtype and weight_dtype must be equal: F32 (all-fp32 path, CUDA-core FMA)
+ * or BF16 (tensor-core path, fp32 accumulation). */
+typedef struct {
+    int64_t T, d, N, M, k_per_group, I;
+    int32_t act_dtype;
+    int32_t weight_dtype;
+} moge_config_t;
+
+/* Optional device outputs of moge_layer_forward; any field may be NULL. */
+typedef struct {
+    float *logits;      /* [T,N] router scores (fp32) */
+    int32_t *topk_idx;  /* [T,K] */
+    float *topk_gate;   /* [T,K] */
+    int32_t *counts;    /* [N] */
+    int32_t *offsets;   /* [N+1] */
+    int32_t *group_load;/* [M] */
+    float *score;       /* imbalance score, one float */
+} moge_aux_t;
+
+/* ABI version of the loaded library (MOGE_ABI_VERSION at build time). */
+int moge_abi_version(void);
+
+/* Static text for a status code. */
+const char *moge_status_string(moge_status_t s);
+
+/* Bytes of scratch needed by every call below for this configuration
+ * (0 when cfg is invalid).  One workspace may serve all calls of a layer in
+ * stream order.  The first 256 bytes hold the device status word, which
+ * must be zero before first use (see moge_reset_device_status). */
+size_t moge_workspace_bytes(const moge_config_t *cfg);
+
+/* Zero the device status word at the start of ws (enqueued on stream). */
+moge_status_t moge_reset_device_status(void *ws, moge_stream_t stream);
+
+/* Synchronise `stream`, then read the status word at the start of ws:
+ * MOGE_OK, or MOGE_ERR_TIMEOUT if a bounded device wait gave up since the
+ * last reset, or MOGE_ERR_CUDA if the read itself failed. */
+moge_status_t moge_query_device_status(const void *ws, moge_stream_t stream);
+
+/* Routing: router scores -> global softmax -> selection.
+ * Defined by the Pangu Pro MoE explainer, section 1: scores for all N
+ * experts, one softmax over all of them, then top-K' inside each group
+ * (MOGE_ROUTE_GROUPED) or, for the conventional MoE it is compared with,
+ * top-K over all experts (MOGE_ROUTE_GLOBAL_TOPK).
+ *   x        [T,d] or NULL.  If NULL, `logits` is the INPUT [T,N] fp32.
+ *   w_router [N,d] (ignored when x is NULL); bias [N] fp32 or NULL, added to
+ *            the scores before the softmax.
+ *   logits   [T,N] fp32: input when x is NULL, else an optional output (NULL
+ *            to skip).
+ *   topk_idx [T,K] out: expert ids.  GROUPED: slot g*K'+r holds the r-th best
+ *            expert of group g (groups are the contiguous ranges [gG,(g+1)G)).
+ *            GLOBAL_TOPK: slot r holds the r-th best expert overall.
+ *            "Best" compares fp32 scores; equal scores go to the lower index.
+ *   topk_gate[T,K] out: the global softmax probability of each selected
+ *            expert (not renormalised over the selection).
+ * Needs ws (moge_workspace_bytes). */
+moge_status_t moge_route(const moge_config_t *cfg, moge_route_mode_t mode, const void *x,
+                         const void *w_router, const float *bias, float *logits, int32_t *topk_idx,
+                         float *topk_gate, void *ws, size_t ws_bytes, moge_stream_t stream);
+
+/* Permutation of the T*K (token, slot) pairs into expert-contiguous rows
+ * (histogram + prefix sum + deterministic scatter).  Works for either
+ * routing mode: it only needs every token's K experts to be distinct ids in
+ * [0,N) (an id outside that range is skipped and sets no output row).
+ *   counts[e]     = number of pairs routed to expert e
+ *   offsets[e]    = counts[0] + ... + counts[e-1];  offsets[N] = P
+ *   pair_row[t,k] = offsets[e] + #{t' < t routed to e}, e = topk_idx[t,k]
+ *   row_token[r]  = token of row r
+ *   x_perm[r,:]   = x[row_token[r],:]   (skipped when x or x_perm is NULL)
+ * row_token and pair_row may be NULL when not wanted. */
+moge_status_t moge_permute(const moge_config_t *cfg, const int32_t *topk_idx, const void *x,
+                           int32_t *counts, int32_t *offsets, int32_t *pair_row, int32_t *row_token,
+                           void *x_perm, void *ws, size_t ws_bytes, moge_stream_t stream);
+
+/* Grouped expert FFN over the permuted rows (SwiGLU; bf16 on tcgen05 tensor
+ * cores with TMEM accumulators, fp32 on CUDA cores).  For every expert e and
+ * row r in [offsets[e], offsets[e+1]):
+ *   h[r,:]      = silu(x_perm[r,:] W_gate[e]^T) * (x_perm[r,:] W_up[e]^T)
+ *   y_perm[r,:] = h[r,:] W_down[e]^T
+ * with fp32 accumulation; for bf16, h is rounded to bf16 before the down
+ * projection and y_perm is bf16.  `offsets` is read on the device only.
+ * Needs ws (h lives there). */
+moge_status_t moge_expert_ffn(const moge_config_t *cfg, const void *x_perm, const int32_t *offsets,
+                              const void *w_gate, const void *w_up, const void *w_down, void *y_perm,
+                              void *ws, size_t ws_bytes, moge_stream_t stream);
+
+/* Weighted combine in fixed slot order with fp32 accumulation:
+ *   y[t,:] = sum_{k=0..K-1} topk_gate[t,k] * y_perm[pair_row[t,k],:]
+ * rounded once to the activation dtype. */
+moge_status_t moge_combine(const moge_config_t *cfg, const void *y_perm, const int32_t *pair_row,
+                           const float *topk_gate, void *y, moge_stream_t stream);
+
+/* Imbalance score (Pangu Pro MoE explainer, section 1: load of the busiest
+ * device minus load of the idlest over a batch; one group = one device),
+ * normalised by the token count:
+ *   group_load[g] = sum of counts[e] over e in [gG,(g+1)G)
+ *   score         = (max_g group_load[g] - min_g group_load[g]) / T   (fp32 division)
+ * group_load may be NULL. */
+moge_status_t moge_imbalance_score(const moge_config_t *cfg, const int32_t *counts,
+                                   int32_t *group_load, float *score, moge_stream_t stream);
+
+/* The whole layer: moge_route(GROUPED) -> moge_permute -> moge_expert_ffn ->
+ * moge_combine, plus moge_imbalance_score when aux->score or aux->group_load
+ * is set.  x [T,d] in, y [T,d] out; aux (or any of its fields) may be NULL. */
+moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const void *w_router,
+                                 const float *bias, const void *w_gate, const void *w_up,
+                                 const void *w_down, void *y, const moge_aux_t *aux, void *ws,
+                                 size_t ws_bytes, moge_stream_t stream);
+
+/* ---- Instrumentation (no counterpart on the pages: measurement support) ---- */
+
+/* Stages of moge_layer_forward, in launch order. */
+typedef enum {
+    MOGE_STAGE_ROUTE = 0,     /* router projection + softmax + selection */
+    MOGE_STAGE_PERMUTE = 1,   /* histogram + prefix sum + scatter */
+    MOGE_STAGE_GATHER = 2,    /* x rows -> x_perm */
+    MOGE_STAGE_GATE_UP = 3,   /* grouped GEMM with W_gate/W_up + SwiGLU -> h */
+    MOGE_STAGE_DOWN = 4,      /* grouped GEMM with W_down -> y_perm */
+    MOGE_STAGE_COMBINE = 5,   /* weighted combine -> y */
+    MOGE_STAGE_IMBALANCE = 6, /* group loads + imbalance score (may be empty) */
+    MOGE_NUM_STAGES = 7
+} moge_stage_t;
+
+/* Ask moge_layer_forward (on the calling host thread) to record events[i]
+ * (cudaEvent_t handles owned by the caller) on its stream right before stage i
+ * and events[MOGE_NUM_STAGES] after the last stage, so that
+ * cudaEventElapsedTime(events[i], events[i+1]) is the device time of stage i.
+ * n must be MOGE_NUM_STAGES + 1; events == NULL turns recording off.  The
+ * array is read at each call, so it must stay valid while recording is on. */
+moge_status_t moge_set_stage_events(void *const *events, int n);
+
+/* Number of kernels this library has launched since it was loaded (all host
+ * threads).  Lets a caller count the device work behind a region of calls. */
+uint64_t moge_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOGE_H */

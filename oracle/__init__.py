@@ -62,6 +62,7 @@ def _get():
             lib.oracle_expert_ffn_pairs.argtypes = [i64, vp, vp, i64, i64, c_int, vp, vp, vp, vp, vp]
             lib.oracle_combine_tokens.argtypes = [i64, vp, i64, vp, vp, i64, i64, c_int, vp, vp, vp,
                                                   vp, vp]
+            lib.oracle_combine_rows.argtypes = [i64, i64, i64, c_int, vp, vp, vp, vp]
             _lib = lib
     return _lib
 
@@ -196,6 +197,20 @@ def combine_tokens(tokens, idx, gate64, x, w_gate, w_up, w_down) -> np.ndarray:
     _get().oracle_combine_tokens(tokens.shape[0], tokens.ctypes.data, K, idx.ctypes.data,
                                  gate64.ctypes.data, d, I, dt, x.ctypes.data, w_gate.ctypes.data,
                                  w_up.ctypes.data, w_down.ctypes.data, y.ctypes.data)
+    return y
+
+
+def combine_rows(rows, pair_row, gate64) -> np.ndarray:
+    """y [T, d] float64 = sum_k gate[t,k] * rows[pair_row[t,k]] (the combine step alone)."""
+    dt = _dt(rows)
+    rows = np.ascontiguousarray(rows)
+    pair_row = _c(pair_row, np.int32)
+    gate64 = _c(gate64, np.float64)
+    T, K = pair_row.shape
+    d = rows.shape[1]
+    y = np.empty((T, d), dtype=np.float64)
+    _get().oracle_combine_rows(T, K, d, dt, rows.ctypes.data, pair_row.ctypes.data, gate64.ctypes.data,
+                               y.ctypes.data)
     return y
 
 

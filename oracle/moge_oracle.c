@@ -264,3 +264,20 @@ void oracle_combine_tokens(int64_t n_tok, const int32_t *tokens, int64_t K, cons
         free(o);
     }
 }
+
+/* The combine step alone, on given expert-output rows (reading: gates weight
+ * the expert outputs, summed in slot order):
+ *   y[t,:] = sum_k gate[t,k] * rows[pair_row[t,k], :]   (double; rows of any dtype). */
+void oracle_combine_rows(int64_t T, int64_t K, int64_t d, int dtype, const void *rows, const int32_t *pair_row,
+                         const double *gate64, double *y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double *yt = y + t * d;
+        for (int64_t j = 0; j < d; ++j) yt[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t r = pair_row[t * K + k];
+            const double g = gate64[t * K + k];
+            for (int64_t j = 0; j < d; ++j) yt[j] += g * val(rows, dtype, r * d + j);
+        }
+    }
+}

@@ -1,0 +1,99 @@
+// Shared device/host helpers of the MoGE CUDA library (internal header).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moge.h"
+
+namespace moge {
+
+// Kernel launch counter and per-thread stage events (instrumentation, api.cu).
+void count_launches(int n);
+void mark_stage(int stage, cudaStream_t s);
+
+// Status word bits (first 4 bytes of the workspace).
+enum : uint32_t {
+    kStatusTimeout = 1u << 0,   // a bounded mbarrier wait gave up
+    kStatusBadIndex = 1u << 1,  // an expert id outside [0, N) was skipped
+};
+
+__device__ __forceinline__ void raise_status(uint32_t *status, uint32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+__host__ __device__ constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+// SwiGLU activation silu(a) * u with silu(a) = a / (1 + exp(-a)).
+// swiglu_fast uses the hardware exp2 approximation (bf16 tensor-core path, whose
+// output is rounded to bf16 anyway); swiglu_precise uses expf (all-fp32 path).
+__device__ __forceinline__ float swiglu_fast(float a, float u) { return a / (1.0f + __expf(-a)) * u; }
+__device__ __forceinline__ float swiglu_precise(float a, float u) { return a / (1.0f + expf(-a)) * u; }
+
+// ---------------------------------------------------------------------------------------------
+// Workspace layout (every region 256-byte aligned).  Computed identically on every call.
+// ---------------------------------------------------------------------------------------------
+struct WsLayout {
+    size_t status, logits, idx, gate, counts, offsets, pair_row, row_token, chunk_counts, sched,
+        x_perm, h, y_perm, total;
+};
+
+constexpr int kPermuteChunk = 256;   // tokens per permutation block
+
+inline WsLayout ws_layout(const moge_config_t &c) {
+    const int64_t K = c.M * c.k_per_group;
+    const int64_t P = c.T * K;
+    const size_t es = (c.act_dtype == MOGE_BF16) ? 2 : 4;
+    const int64_t chunks = cdiv(c.T > 0 ? c.T : 1, kPermuteChunk);
+    WsLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off += (size_t)round_up((int64_t)bytes, 256); return o; };
+    L.status = take(256);
+    L.logits = take((size_t)c.T * c.N * 4);
+    L.idx = take((size_t)P * 4);
+    L.gate = take((size_t)P * 4);
+    L.counts = take((size_t)c.N * 4);
+    L.offsets = take((size_t)(c.N + 1) * 4);
+    L.pair_row = take((size_t)P * 4);
+    L.row_token = take((size_t)P * 4);
+    L.chunk_counts = take((size_t)chunks * c.N * 4);
+    L.sched = take(64 * 1024);
+    L.x_perm = take((size_t)P * c.d * es);
+    L.h = take((size_t)P * c.I * es);
+    L.y_perm = take((size_t)P * c.d * es);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Launchers (defined in the .cu files).  All return cudaGetLastError() after launching.
+// ---------------------------------------------------------------------------------------------
+cudaError_t launch_route_select(const float *logits, int64_t T, int64_t N, int64_t M, int64_t kpg,
+                                bool global, int32_t *idx, float *gate, cudaStream_t s);
+cudaError_t launch_router_logits_simt(const void *x, const void *w_r, const float *bias, int64_t T,
+                                      int64_t d, int64_t N, int dtype, float *logits, cudaStream_t s);
+cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, int32_t *counts,
+                           int32_t *offsets, int32_t *pair_row, int32_t *row_token, int32_t *chunk_counts,
+                           uint32_t *status, cudaStream_t s);
+cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const int32_t *offsets,
+                               int64_t N, int64_t P, int64_t d, int dtype, void *x_perm, cudaStream_t s);
+cudaError_t launch_imbalance(const int32_t *counts, int64_t T, int64_t N, int64_t M, int32_t *group_load,
+                             float *score, cudaStream_t s);
+cudaError_t launch_combine(const void *y_perm, const int32_t *pair_row, const float *gate, int64_t T,
+                           int64_t K, int64_t d, int dtype, void *y, cudaStream_t s);
+cudaError_t launch_ffn_simt(const void *x_perm, const int32_t *offsets, int64_t N, int64_t P, int64_t d,
+                            int64_t I, int dtype, const void *w_gate, const void *w_up, const void *w_down,
+                            void *h, void *y_perm, cudaStream_t s);
+
+}  // namespace moge

@@ -1,0 +1,264 @@
+// Permutation of (token, slot) pairs into expert-contiguous rows:
+// histogram -> prefix sum -> deterministic scatter, then the row gather.
+//
+// Row of pair (t,k) with expert e:  offsets[e] + #{t' < t routed to e}.
+// Tokens are cut into chunks of kPermuteChunk (one block each, one token per
+// thread).  Inside a chunk, warp w publishes, for every expert, the bitmask of
+// its lanes routed there (shared atomicOr: order-free, so deterministic); the
+// rank of a lane among earlier lanes is popc(mask & lanemask_lt), the rank of a
+// warp's first lane is the sum of popc over earlier warps, and the chunk's base
+// is the sum over earlier chunks.  A token selects each expert at most once, so
+// "earlier pair with the same expert" equals "earlier token".
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace moge {
+
+constexpr int kChunk = kPermuteChunk;
+constexpr int kWarps = kChunk / 32;
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Fill masks[w*N + e] for this block's chunk.  Returns nothing; caller syncs.
+__device__ __forceinline__ void build_masks(const int32_t *__restrict__ idx, int64_t T, int K, int N,
+                                            uint32_t *masks, uint32_t *status) {
+    for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) masks[i] = 0u;
+    __syncthreads();
+    const int64_t t = (int64_t)blockIdx.x * kChunk + threadIdx.x;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (t < T) {
+        for (int k = 0; k < K; ++k) {
+            const int e = idx[t * K + k];
+            if (e >= 0 && e < N) atomicOr(&masks[w * N + e], 1u << lane);
+            else raise_status(status, kStatusBadIndex);
+        }
+    }
+}
+
+// Per-chunk expert counts: chunk_counts[chunk][e].
+__global__ void permute_count_kernel(const int32_t *__restrict__ idx, int64_t T, int K, int N,
+                                     int32_t *__restrict__ chunk_counts, uint32_t *status) {
+    extern __shared__ uint32_t masks[];  // [kWarps][N]
+    build_masks(idx, T, K, N, masks, status);
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int c = 0;
+        for (int w = 0; w < kWarps; ++w) c += __popc(masks[w * N + e]);
+        chunk_counts[(int64_t)blockIdx.x * N + e] = c;
+    }
+}
+
+// One block: chunk_counts -> per-chunk bases (in place), counts, offsets.
+__global__ void permute_scan_kernel(int32_t *__restrict__ chunk_counts, int chunks, int N,
+                                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets) {
+    extern __shared__ int32_t tot[];  // [N]
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < chunks; ++c) {
+            const int v = chunk_counts[(int64_t)c * N + e];
+            chunk_counts[(int64_t)c * N + e] = run;
+            run += v;
+        }
+        tot[e] = run;
+        counts[e] = run;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // N <= 1024: a serial scan is cheap and obviously ordered
+        int run = 0;
+        for (int e = 0; e < N; ++e) {
+            offsets[e] = run;
+            run += tot[e];
+        }
+        offsets[N] = run;
+    }
+}
+
+// Rows of the chunk's pairs.  base[e] = offsets[e] + bases of earlier chunks.
+__device__ __forceinline__ void scatter_rows(const int32_t *__restrict__ idx, int64_t T, int K, int N,
+                                             const uint32_t *masks, int32_t *warp_base,
+                                             const int32_t *base, int32_t *__restrict__ pair_row,
+                                             int32_t *__restrict__ row_token) {
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int run = base[e];
+        for (int w = 0; w < kWarps; ++w) {
+            warp_base[w * N + e] = run;
+            run += __popc(masks[w * N + e]);
+        }
+    }
+    __syncthreads();
+    const int64_t t = (int64_t)blockIdx.x * kChunk + threadIdx.x;
+    const int w = threadIdx.x >> 5;
+    const uint32_t lt = lanemask_lt();
+    if (t < T) {
+        for (int k = 0; k < K; ++k) {
+            const int e = idx[t * K + k];
+            int row = -1;
+            if (e >= 0 && e < N) row = warp_base[w * N + e] + __popc(masks[w * N + e] & lt);
+            if (pair_row) pair_row[t * K + k] = row;
+            if (row_token && row >= 0) row_token[row] = (int32_t)t;
+        }
+    }
+}
+
+__global__ void permute_scatter_kernel(const int32_t *__restrict__ idx, int64_t T, int K, int N,
+                                       const int32_t *__restrict__ chunk_base,
+                                       const int32_t *__restrict__ offsets, int32_t *__restrict__ pair_row,
+                                       int32_t *__restrict__ row_token) {
+    extern __shared__ uint32_t sm[];
+    uint32_t *masks = sm;                              // [kWarps][N]
+    int32_t *warp_base = (int32_t *)(sm + kWarps * N);  // [kWarps][N]
+    int32_t *base = warp_base + kWarps * N;             // [N]
+    build_masks(idx, T, K, N, masks, nullptr);
+    for (int e = threadIdx.x; e < N; e += blockDim.x)
+        base[e] = offsets[e] + chunk_base[(int64_t)blockIdx.x * N + e];
+    __syncthreads();
+    scatter_rows(idx, T, K, N, masks, warp_base, base, pair_row, row_token);
+}
+
+// T <= kChunk: count, scan and scatter in one block.
+__global__ void permute_single_kernel(const int32_t *__restrict__ idx, int64_t T, int K, int N,
+                                      int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                      int32_t *__restrict__ pair_row, int32_t *__restrict__ row_token,
+                                      uint32_t *status) {
+    extern __shared__ uint32_t sm[];
+    uint32_t *masks = sm;
+    int32_t *warp_base = (int32_t *)(sm + kWarps * N);
+    int32_t *base = warp_base + kWarps * N;
+    build_masks(idx, T, K, N, masks, status);
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int c = 0;
+        for (int w = 0; w < kWarps; ++w) c += __popc(masks[w * N + e]);
+        base[e] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int e = 0; e < N; ++e) {
+            const int c = base[e];
+            counts[e] = c;
+            offsets[e] = run;
+            base[e] = run;
+            run += c;
+        }
+        offsets[N] = run;
+    }
+    __syncthreads();
+    scatter_rows(idx, T, K, N, masks, warp_base, base, pair_row, row_token);
+}
+
+__global__ void zero_counts_kernel(int N, int32_t *counts, int32_t *offsets) {
+    for (int e = threadIdx.x; e <= N; e += blockDim.x) {
+        if (e < N) counts[e] = 0;
+        offsets[e] = 0;
+    }
+}
+
+cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, int32_t *counts,
+                           int32_t *offsets, int32_t *pair_row, int32_t *row_token, int32_t *chunk_counts,
+                           uint32_t *status, cudaStream_t s) {
+    if (T == 0) {
+        zero_counts_kernel<<<1, 256, 0, s>>>((int)N, counts, offsets);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    const size_t smem_scatter = (size_t)(2 * kWarps * N + N) * 4;
+    cudaError_t err;
+    if (T <= kChunk) {
+        err = cudaFuncSetAttribute(permute_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem_scatter);
+        if (err != cudaSuccess) return err;
+        permute_single_kernel<<<1, kChunk, smem_scatter, s>>>(idx, T, (int)K, (int)N, counts, offsets,
+                                                              pair_row, row_token, status);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    const int chunks = (int)cdiv(T, kChunk);
+    const size_t smem_count = (size_t)kWarps * N * 4;
+    err = cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_count);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_scatter);
+    if (err != cudaSuccess) return err;
+    permute_count_kernel<<<chunks, kChunk, smem_count, s>>>(idx, T, (int)K, (int)N, chunk_counts, status);
+    count_launches(1);
+    permute_scan_kernel<<<1, 1024, (size_t)N * 4, s>>>(chunk_counts, chunks, (int)N, counts, offsets);
+    count_launches(1);
+    permute_scatter_kernel<<<chunks, kChunk, smem_scatter, s>>>(idx, T, (int)K, (int)N, chunk_counts,
+                                                                offsets, pair_row, row_token);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Row gather x_perm[r,:] = x[row_token[r],:]; one warp per row, 16-byte vectors.
+// Only rows r < offsets[N] (the pairs that exist) are copied.
+// ---------------------------------------------------------------------------------------------
+__global__ void gather_rows_kernel(const int4 *__restrict__ x, const int32_t *__restrict__ row_token,
+                                   const int32_t *__restrict__ offsets, int N, int64_t vec_per_row,
+                                   int4 *__restrict__ x_perm) {
+    const int64_t rows = offsets[N];
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = warp; r < rows; r += nwarps) {
+        const int64_t t = row_token[r];
+        const int4 *src = x + t * vec_per_row;
+        int4 *dst = x_perm + r * vec_per_row;
+        for (int64_t v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const int32_t *offsets, int64_t N,
+                               int64_t P, int64_t d, int dtype, void *x_perm, cudaStream_t s) {
+    if (P == 0) return cudaSuccess;
+    const int64_t row_bytes = d * (dtype == MOGE_BF16 ? 2 : 4);
+    const int64_t vec = row_bytes / 16;
+    int sms = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = cdiv(P, 8);  // 8 warps (rows in flight) per block
+    const unsigned blocks = (unsigned)std::min<int64_t>(want, (int64_t)sms * 8);
+    gather_rows_kernel<<<blocks, 256, 0, s>>>((const int4 *)x, row_token, offsets, (int)N, vec, (int4 *)x_perm);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Imbalance score: group loads, then (max - min) / T.  One block.
+// ---------------------------------------------------------------------------------------------
+__global__ void imbalance_kernel(const int32_t *__restrict__ counts, int64_t T, int N, int M,
+                                 int32_t *__restrict__ group_load, float *__restrict__ score) {
+    extern __shared__ int64_t loads[];  // [M]
+    const int G = N / M;
+    for (int g = threadIdx.x; g < M; g += blockDim.x) {
+        int64_t sum = 0;
+        for (int e = g * G; e < (g + 1) * G; ++e) sum += counts[e];
+        loads[g] = sum;
+        if (group_load) group_load[g] = (int32_t)sum;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && score) {
+        int64_t mx = loads[0], mn = loads[0];
+        for (int g = 1; g < M; ++g) {
+            mx = max(mx, loads[g]);
+            mn = min(mn, loads[g]);
+        }
+        *score = (T > 0) ? (float)(mx - mn) / (float)T : 0.f;
+    }
+}
+
+cudaError_t launch_imbalance(const int32_t *counts, int64_t T, int64_t N, int64_t M, int32_t *group_load,
+                             float *score, cudaStream_t s) {
+    imbalance_kernel<<<1, 256, (size_t)M * 8, s>>>(counts, T, (int)N, (int)M, group_load, score);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moge

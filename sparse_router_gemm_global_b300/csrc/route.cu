@@ -1,0 +1,143 @@
+// Routing: global softmax over all N experts + top-K' inside each group
+// (Pangu Pro MoE explainer, section 1 "innovative architecture"), and the
+// conventional top-K over all experts it is compared with.
+//
+// One thread routes one token from a shared-memory copy of its N scores
+// (row stride N+1 keeps the per-thread reads bank-conflict free).  The
+// selection compares fp32 scores with equal scores going to the lower expert
+// index, so it is independent of how exp() rounds; the gates are
+// exp(l - max) / sum_e exp(l_e - max) with a compensated fp32 sum.
+#include "common.cuh"
+
+namespace moge {
+
+// Route one token from its scores l[0..N).  groups/G/per describe the
+// selection: GROUPED = (M, N/M, K'), GLOBAL = (1, N, M*K').
+__device__ __forceinline__ void route_token(const float *l, int N, int groups, int G, int per,
+                                            int32_t *idx_out, float *gate_out) {
+    float m = l[0];
+    for (int e = 1; e < N; ++e) m = fmaxf(m, l[e]);
+    // Neumaier-compensated sum of exp(l - m)
+    float s = 0.f, comp = 0.f;
+    for (int e = 0; e < N; ++e) {
+        const float v = expf(l[e] - m);
+        const float t = s + v;
+        comp += (fabsf(s) >= fabsf(v)) ? ((s - t) + v) : ((v - t) + s);
+        s = t;
+    }
+    s += comp;
+    for (int g = 0; g < groups; ++g) {
+        // walk the group's experts in rank order: each round takes the best
+        // expert ranking strictly after the previously taken one
+        float last_v = __int_as_float(0x7f800000);  // +inf
+        int last_e = -1;
+        for (int r = 0; r < per; ++r) {
+            float bv = 0.f;
+            int be = -1;
+            for (int e = g * G; e < (g + 1) * G; ++e) {
+                const float v = l[e];
+                const bool after = (v < last_v) || (v == last_v && e > last_e);
+                if (after && (be < 0 || v > bv)) { bv = v; be = e; }
+            }
+            idx_out[g * per + r] = be;
+            gate_out[g * per + r] = expf(bv - m) / s;
+            last_v = bv;
+            last_e = be;
+        }
+    }
+}
+
+__global__ void route_select_kernel(const float *__restrict__ logits, int T, int N, int groups, int G,
+                                    int per, int32_t *__restrict__ idx, float *__restrict__ gate) {
+    extern __shared__ float tile[];  // [blockDim.x][N+1]
+    const int tpb = blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * tpb;
+    const int ntok = (int)min((int64_t)tpb, (int64_t)T - t0);
+    const int stride = N + 1;
+    const float *src = logits + t0 * N;
+    for (int i = threadIdx.x; i < ntok * N; i += tpb) {
+        const int r = i / N, c = i - r * N;
+        tile[r * stride + c] = src[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < ntok) {
+        const int K = groups * per;
+        const int64_t t = t0 + threadIdx.x;
+        route_token(tile + threadIdx.x * stride, N, groups, G, per, idx + t * K, gate + t * K);
+    }
+}
+
+static int route_tokens_per_block(int64_t N) { return (N <= 639) ? 64 : 32; }
+
+cudaError_t launch_route_select(const float *logits, int64_t T, int64_t N, int64_t M, int64_t kpg,
+                                bool global, int32_t *idx, float *gate, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int tpb = route_tokens_per_block(N);
+    const size_t smem = (size_t)tpb * (N + 1) * sizeof(float);
+    cudaError_t err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    const int groups = global ? 1 : (int)M;
+    const int G = global ? (int)N : (int)(N / M);
+    const int per = global ? (int)(M * kpg) : (int)kpg;
+    route_select_kernel<<<(unsigned)cdiv(T, tpb), tpb, smem, s>>>(logits, (int)T, (int)N, groups, G, per,
+                                                                   idx, gate);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Router projection on CUDA cores: logits[t,e] = sum_i x[t,i] W_r[e,i] + b[e] (fp32 accumulate).
+// 32 tokens x 32 experts per block, 256 threads, 4 outputs per thread, k-chunks of 32.
+// ---------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void router_logits_simt_kernel(const T *__restrict__ x, const T *__restrict__ w,
+                                          const float *__restrict__ bias, int Tn, int d, int N,
+                                          float *__restrict__ logits) {
+    __shared__ float xs[32][33];
+    __shared__ float ws[32][33];
+    const int t0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // ty in [0,8)
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < d; k0 += 32) {
+        for (int i = threadIdx.x; i < 32 * 32; i += 256) {
+            const int r = i >> 5, c = i & 31;
+            const int t = t0 + r, e = e0 + r, k = k0 + c;
+            xs[r][c] = (t < Tn && k < d) ? to_f32(x[(int64_t)t * d + k]) : 0.f;
+            ws[r][c] = (e < N && k < d) ? to_f32(w[(int64_t)e * d + k]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float wv = ws[tx][k];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] = fmaf(xs[ty + 8 * j][k], wv, acc[j]);
+        }
+        __syncthreads();
+    }
+    const int e = e0 + tx;
+    if (e < N) {
+        const float b = bias ? bias[e] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = t0 + ty + 8 * j;
+            if (t < Tn) logits[(int64_t)t * N + e] = acc[j] + b;
+        }
+    }
+}
+
+cudaError_t launch_router_logits_simt(const void *x, const void *w_r, const float *bias, int64_t T,
+                                      int64_t d, int64_t N, int dtype, float *logits, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    dim3 grid((unsigned)cdiv(T, 32), (unsigned)cdiv(N, 32));
+    if (dtype == MOGE_BF16)
+        router_logits_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_r, bias, (int)T, (int)d, (int)N, logits);
+    else
+        router_logits_simt_kernel<float><<<grid, 256, 0, s>>>((const float *)x, (const float *)w_r, bias,
+                                                               (int)T, (int)d, (int)N, logits);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moge

@@ -57,32 +57,36 @@ static inline uint16_t f32_to_bf16_rne(float f) {
     return (uint16_t)(u >> 16);
 }
 
+/* Writes element g of the stream (if it lies in [start, start+count)) to
+ * out[g - start] through put(); pairs are computed once for both elements. */
+#define SYNTH_NORMAL_LOOP(PUT)                                                         \
+    const uint64_t key = stream_key(seed, tensor_id);                                  \
+    if (count == 0) return;                                                            \
+    const int64_t j0 = (int64_t)(start >> 1), j1 = (int64_t)((start + count - 1) >> 1); \
+    _Pragma("omp parallel for schedule(static)")                                       \
+    for (int64_t j = j0; j <= j1; ++j) {                                               \
+        double z[2];                                                                   \
+        normal_pair(key, (uint64_t)j, &z[0], &z[1]);                                   \
+        for (int h = 0; h < 2; ++h) {                                                  \
+            uint64_t g = 2 * (uint64_t)j + (uint64_t)h;                                \
+            if (g < start || g >= start + count) continue;                             \
+            PUT(out[g - start], (float)(stddev * z[h]));                               \
+        }                                                                              \
+    }
+
+#define PUT_F32(dst, v) (dst) = (v)
+#define PUT_BF16(dst, v) (dst) = f32_to_bf16_rne(v)
+
 /* Elements [start, start+count) of the stream, as fp32 (std * N(0,1)). */
 void synth_normal_f32(uint64_t seed, uint64_t tensor_id, uint64_t start, uint64_t count,
                       double stddev, float *out) {
-    const uint64_t key = stream_key(seed, tensor_id);
-    const int64_t n = (int64_t)count;
-#pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < n; ++i) {
-        uint64_t g = start + (uint64_t)i;
-        double z0, z1;
-        normal_pair(key, g >> 1, &z0, &z1);
-        out[i] = (float)(stddev * ((g & 1) ? z1 : z0));
-    }
+    SYNTH_NORMAL_LOOP(PUT_F32)
 }
 
 /* Same stream, rounded on to bf16 (stored as raw uint16 bits). */
 void synth_normal_bf16(uint64_t seed, uint64_t tensor_id, uint64_t start, uint64_t count,
                        double stddev, uint16_t *out) {
-    const uint64_t key = stream_key(seed, tensor_id);
-    const int64_t n = (int64_t)count;
-#pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < n; ++i) {
-        uint64_t g = start + (uint64_t)i;
-        double z0, z1;
-        normal_pair(key, g >> 1, &z0, &z1);
-        out[i] = f32_to_bf16_rne((float)(stddev * ((g & 1) ? z1 : z0)));
-    }
+    SYNTH_NORMAL_LOOP(PUT_BF16)
 }
 
 /* fp32 -> bf16 (nearest-even) for an existing array. */

@@ -1,0 +1,148 @@
+"""GPU parity of the expert FFN, the combine and the whole layer against the oracle.
+
+Tolerances: max|y - ref| <= 2e-2 * max|ref| for bf16 (fp32 accumulation),
+<= 1e-5 * max|ref| for the all-fp32 layer.  End-to-end routing may differ from
+the oracle's only on near-ties (oracle probability gap < 1e-6); such tokens are
+left out of the output comparison and counted.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_router_gemm_global_b300 as moge
+import synth
+from gpu_util import (DEV, as_f64, config, dev, host, max_rel_err, routing_mismatch_ok, run_layer,
+                      torch_dtype, upload_layer)
+from synth import WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f32": 1e-5}
+
+
+def check_layer(w, inp, got, tokens=None, seed_note=""):
+    """Routing of all tokens and outputs of `tokens` (all if None) vs the oracle."""
+    T = w.T
+    ref = oracle.route(oracle.router_logits(inp["x"], inp["w_router"], inp["bias"]), w.M, w.kpg)
+    near = routing_mismatch_ok(got["topk_idx"], ref["idx"], ref["p"], w.M, w.kpg)
+    assert len(near) <= max(2, T // 1000), f"too many near-tie tokens: {len(near)}"
+    # the permutation and loads follow the GPU's own routing exactly
+    perm = oracle.permute(got["topk_idx"], w.N)
+    np.testing.assert_array_equal(got["counts"], perm["counts"])
+    np.testing.assert_array_equal(got["offsets"], perm["offsets"])
+    loads, score = oracle.imbalance(perm["counts"], T, w.M)
+    np.testing.assert_array_equal(got["group_load"], loads)
+    assert got["score"] == 0.0 and np.all(loads == T * w.kpg)
+    # gates: the GPU's fp32 softmax of its own scores vs the oracle's, for agreeing tokens
+    ok = np.array([t not in near for t in range(T)])
+    gate_tol = 2e-4 if w.dtype == "bf16" else 1e-5  # scores differ by accumulation order
+    assert np.max(np.abs(got["topk_gate"][ok] - ref["gate64"][ok])) < gate_tol
+    # outputs
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    toks = np.array([t for t in toks if t not in near], dtype=np.int32)
+    y_ref = oracle.combine_tokens(toks, ref["idx"], ref["gate64"], inp["x"], inp["w_gate"], inp["w_up"],
+                                  inp["w_down"])
+    err = max_rel_err(got["y"][toks], y_ref)
+    assert err <= TOL[w.dtype], f"{w.name}: max rel err {err:.3e} {seed_note}"
+    return err
+
+
+def test_tiny_fp32_layer():
+    w = WORKLOADS["tiny_fp32"]
+    inp = synth.layer_inputs(w)
+    got = run_layer(w, upload_layer(inp))
+    check_layer(w, inp, got)
+    # the fp32 scores themselves: within a few ulp of the oracle's double-then-fp32 scores
+    l_ref = oracle.router_logits(inp["x"], inp["w_router"], inp["bias"])
+    assert np.max(np.abs(got["logits"] - l_ref)) < 1e-5
+
+
+@pytest.mark.parametrize("T,d,N,M,kpg,I", [
+    (300, 256, 16, 4, 2, 192),     # ragged rows and a ragged intermediate tile
+    (129, 512, 32, 8, 1, 256),
+    (1, 128, 16, 4, 4, 64),        # one token, K' = G
+    (64, 384, 24, 1, 3, 320),      # a single group = global top-K
+    (520, 256, 256, 8, 1, 128),    # wide groups (G = 32), many empty experts
+])
+def test_bf16_layer_shapes(T, d, N, M, kpg, I):
+    w = WORKLOADS["decode_t32"].with_(name=f"bf16_{T}_{d}_{N}_{M}_{kpg}_{I}", T=T, d=d, N=N, M=M, kpg=kpg, I=I)
+    inp = synth.layer_inputs(w, seed=T + d + N)
+    got = run_layer(w, upload_layer(inp))
+    check_layer(w, inp, got)
+
+
+def test_decode_t32_full():
+    w = WORKLOADS["decode_t32"]
+    inp = synth.layer_inputs(w)
+    got = run_layer(w, upload_layer(inp))
+    check_layer(w, inp, got)
+
+
+def test_prefill_t8192_sampled():
+    w = WORKLOADS["prefill_t8192"]
+    inp = synth.layer_inputs(w)
+    got = run_layer(w, upload_layer(inp))
+    rng = np.random.default_rng(1)
+    toks = np.sort(np.concatenate([[0, w.T - 1], rng.choice(w.T, 46, replace=False)]))
+    check_layer(w, inp, got, tokens=toks)
+
+
+def test_layer_is_deterministic():
+    w = WORKLOADS["decode_t32"].with_(T=700, d=512, I=256)
+    d_inp = upload_layer(synth.layer_inputs(w, seed=21))
+    a = run_layer(w, d_inp)
+    b = run_layer(w, d_inp)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+def test_expert_ffn_and_combine_on_oracle_permutation():
+    """moge_expert_ffn on the oracle's own permutation, then moge_combine, each vs the oracle."""
+    w = WORKLOADS["decode_t32"].with_(T=333, d=256, I=192)
+    inp = synth.layer_inputs(w, seed=5)
+    ref = oracle.layer_forward(inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                               inp["w_down"], w.M, w.kpg)
+    c = config(w)
+    ws = moge.alloc_workspace(c)
+    x_perm = dev(inp["x"][ref["row_token"]])
+    y_perm = torch.empty((w.P, w.d), dtype=torch.bfloat16, device=DEV)
+    d_inp = upload_layer(inp)
+    moge.moge_expert_ffn(c, x_perm, dev(ref["offsets"]), d_inp["w_gate"], d_inp["w_up"], d_inp["w_down"],
+                         y_perm, ws)
+    torch.cuda.synchronize()
+    yp = host(y_perm)
+    experts = np.repeat(np.arange(w.N, dtype=np.int32), ref["counts"])
+    rows_ref = oracle.expert_ffn_pairs(ref["row_token"], experts, inp["x"], inp["w_gate"], inp["w_up"],
+                                       inp["w_down"])
+    assert max_rel_err(yp, rows_ref) <= TOL["bf16"]
+    # combine of the GPU rows vs the oracle's combine of the same rows
+    y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=DEV)
+    moge.moge_combine(c, y_perm, dev(ref["pair_row"]), dev(ref["gate"]), y)
+    torch.cuda.synchronize()
+    y_ref = oracle.combine_rows(yp, ref["pair_row"], ref["gate"].astype(np.float64))
+    # fp32 accumulation of bf16 rows, one final bf16 rounding: within 2 bf16 ulps
+    assert np.max(np.abs(as_f64(host(y)) - y_ref) / (np.abs(y_ref) + 1e-3)) < 2 ** -7
+
+
+def test_empty_layer():
+    w = WORKLOADS["decode_t32"].with_(T=0)
+    c = config(w)
+    ws = moge.alloc_workspace(c)
+    d_inp = upload_layer(synth.layer_inputs(w.with_(T=1)))
+    y = torch.empty((0, w.d), dtype=torch.bfloat16, device=DEV)
+    counts = torch.full((w.N,), 3, dtype=torch.int32, device=DEV)
+    moge.moge_layer_forward(c, d_inp["x"], d_inp["w_router"], d_inp["bias"], d_inp["w_gate"], d_inp["w_up"],
+                            d_inp["w_down"], y, ws, aux={"counts": counts})
+    torch.cuda.synchronize()
+    assert np.all(host(counts) == 0)
+
+
+@pytest.mark.slow
+def test_stress_n256_sampled():
+    w = WORKLOADS["stress_n256"]
+    inp = synth.layer_inputs(w)
+    got = run_layer(w, upload_layer(inp))
+    rng = np.random.default_rng(2)
+    toks = np.sort(rng.choice(w.T, 24, replace=False))
+    check_layer(w, inp, got, tokens=toks)

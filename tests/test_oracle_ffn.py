@@ -128,3 +128,19 @@ def test_planted_renormalised_gates_mistake_is_caught():
     r = oracle.route(oracle.router_logits(inp["x"], inp["w_router"]), w.M, w.kpg)
     renorm = r["gate64"] / r["gate64"].sum(axis=1, keepdims=True)
     assert np.max(np.abs(renorm.sum(axis=1) - r["gate64"].sum(axis=1))) > 0.1
+
+
+def test_combine_rows_equals_per_token_combine():
+    # the combine step applied to permuted expert outputs gives the per-token combine
+    w = WORKLOADS["tiny_fp32"].with_(T=20, d=32, I=16)
+    inp = synth.layer_inputs(w, seed=9)
+    r = oracle.layer_forward(inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                             inp["w_down"], w.M, w.kpg)
+    rows = oracle.expert_ffn_pairs(r["row_token"], np.repeat(np.arange(w.N), r["counts"]), inp["x"],
+                                   inp["w_gate"], inp["w_up"], inp["w_down"])
+    y = oracle.combine_rows(rows.astype(np.float32), r["pair_row"], r["gate64"])
+    assert np.max(np.abs(y - r["y"])) < 1e-6 * np.max(np.abs(r["y"]))
+    # hand case: two rows, weights 0.5 and 2
+    rows2 = np.array([[1.0, -2.0], [4.0, 0.5]], dtype=np.float32)
+    y2 = oracle.combine_rows(rows2, np.array([[1, 0]]), np.array([[0.5, 2.0]]))
+    assert np.array_equal(y2, np.array([[4.0, -3.75]]))
