@@ -1,14 +1,526 @@
-// Grouped expert FFN, bf16 path (bring-up: CUDA-core kernel until the tensor-core kernel lands).
+// Grouped expert SwiGLU FFN on 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Two persistent launches per layer (gate/up + SwiGLU -> h, then down -> y_perm), each with
+// one CTA per SM walking a tile list derived on the device from the expert offsets (no host
+// round trip).  Per CTA: warp 0 issues TMA loads into a shared-memory ring, warp 1 issues
+// tcgen05.mma from one thread into a double-buffered TMEM accumulator, warp 2 owns the TMEM
+// allocation, warps 4-7 drain TMEM (tcgen05.ld), apply the epilogue and store bf16.
+//
+// Tile shapes (M x N x K = rows of operand A x rows of operand B x 64 per k-block):
+//   tokens-as-M (many tokens per expert, prefill):
+//     gate/up: A = 128 permuted token rows, B = 128 W_gate rows stacked on the matching
+//              128 W_up rows (one N=256 MMA); epilogue h = silu(acc[:, :128]) * acc[:, 128:].
+//     down:    A = 128 h rows, B = 256 W_down rows; epilogue y_perm = acc.
+//   weights-as-M ("swap", few tokens per expert, decode): A = 128 weight rows, B = the
+//     expert's (<= 64) token rows, so the weights stream at full MMA height; gate/up issue one
+//     MMA for W_gate and one for W_up into two TMEM column ranges.
+// Rows of a tile never belong to two experts: the tile list is built per expert, rows past
+// the expert's count (or past the tensor) are loaded (other experts' rows or TMA zero fill)
+// but never stored.
+//
+// Every mbarrier wait is bounded (kTimeoutNs).  A wait that gives up sets the workspace
+// status word (MOGE_ERR_TIMEOUT through moge_query_device_status), raises a CTA-wide abort
+// flag that ends the other roles' loops, drains the copies and MMAs it issued and frees TMEM
+// before the CTA exits.
+#include <cudaTypedefs.h>
+#include <mutex>
+
 #include "ffn_tc.cuh"
+#include "tc_ptx.cuh"
 
 namespace moge {
+namespace tc {
 
-cudaError_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, int64_t N, int64_t P, int64_t T,
-                          int64_t d, int64_t I, const void *w_gate, const void *w_up, const void *w_down,
-                          void *h, void *y_perm, uint32_t *status, cudaStream_t s) {
-    (void)T;
-    (void)status;
-    return launch_ffn_simt(x_perm, offsets, N, P, d, I, MOGE_BF16, w_gate, w_up, w_down, h, y_perm, s);
+using namespace ptx;
+
+constexpr int kBM = 128;            // MMA M
+constexpr int kBK = 64;             // k-block: 64 bf16 = 128 bytes = one 128B-swizzle row
+constexpr int kThreads = 256;       // 8 warps
+constexpr int kEpiWarp0 = 4;        // epilogue warps 4..7 (TMEM lane quarter = warp % 4)
+constexpr int kMaxExperts = 1024;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int kSmemBudget = 220 * 1024;
+
+enum Mode { NORMAL_GLU = 0, NORMAL_PLAIN = 1, SWAP_GLU = 2, SWAP_PLAIN = 3 };
+
+template <int MODE, int BNT>
+struct Cfg {
+    static constexpr bool swap = (MODE == SWAP_GLU || MODE == SWAP_PLAIN);
+    static constexpr bool glu = (MODE == NORMAL_GLU || MODE == SWAP_GLU);
+    static constexpr int mma_n = swap ? BNT : 256;                      // MMA N (rows of operand B)
+    static constexpr int tok_block = swap ? BNT : kBM;                  // tokens per tile
+    static constexpr int feat_block = (swap || glu) ? 128 : 256;        // output features per tile
+    static constexpr int a_tiles = (swap && glu) ? 2 : 1;               // W_gate + W_up as two A tiles
+    static constexpr int a_bytes = kBM * 128;                           // one 128-row A tile
+    static constexpr int b_bytes = mma_n * 128;
+    static constexpr int stage_bytes = a_tiles * a_bytes + b_bytes;
+    static constexpr int stages_raw = kSmemBudget / stage_bytes;
+    static constexpr int stages = stages_raw > 12 ? 12 : stages_raw;
+    static constexpr int acc_cols = swap ? (glu ? 2 * BNT : BNT) : 256;  // fp32 columns per accumulator
+    static constexpr int tmem_cols = (2 * acc_cols <= 32) ? 32 : (2 * acc_cols <= 64) ? 64
+                                   : (2 * acc_cols <= 128) ? 128 : (2 * acc_cols <= 256) ? 256 : 512;
+    static constexpr uint32_t idesc = idesc_bf16_f32(kBM, mma_n);
+    static constexpr size_t smem_bytes = (size_t)stages * stage_bytes + 1024;  // + alignment slack
+    static_assert(stage_bytes % 1024 == 0, "stage tiles must keep 1024-byte alignment");
+    static_assert(stages >= 2, "pipeline needs two stages");
+};
+
+struct Params {
+    const int32_t *offsets;  // [N+1] expert row offsets (device)
+    int N;                   // experts
+    int kdim;                // reduction length (d for gate/up, I for down)
+    int out_dim;             // output features (I for gate/up, d for down)
+    __nv_bfloat16 *out;      // [P, out_dim]
+    uint32_t *status;        // workspace status word
+};
+
+// Bounded wait.  Returns false (and raises the abort flag) if it gives up.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         uint32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 31) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs || n > (1u << 30)) {
+                *abort_flag = 1;
+                raise_status(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: used at exit for copies and MMAs already issued.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t *status) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 0; !mbar_try_wait(bar, parity); ++n) {
+        if ((n & 31) == 31 && (globaltimer() - t0 > kTimeoutNs || n > (1u << 30))) {
+            raise_status(status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+// prefix[e] = sum over e' < e of ceil(count_e' / tok_block); all 256 threads, N <= 1024.
+__device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int tok_block, int32_t *prefix,
+                             int32_t *warp_sums) {
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    int v[4];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = t * 4 + i;
+        int b = 0;
+        if (e < N) b = (offsets[e + 1] - offsets[e] + tok_block - 1) / tok_block;
+        local += b;
+        v[i] = local;
+    }
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int s = lane < 8 ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < 8) warp_sums[lane] = s;
+    }
+    __syncthreads();
+    const int excl = x - local + (w > 0 ? warp_sums[w - 1] : 0);
+    if (t == 0) prefix[0] = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = t * 4 + i;
+        if (e < N) prefix[e + 1] = excl + v[i];
+    }
+    __syncthreads();
+}
+
+// tile -> (expert, token block inside the expert, feature block)
+__device__ __forceinline__ void tile_coords(int tile, int nfb, const int32_t *prefix, int N, int &e, int &tb,
+                                            int &fb) {
+    const int tbg = tile / nfb;
+    fb = tile - tbg * nfb;
+    int lo = 0, hi = N - 1;  // last e with prefix[e] <= tbg
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= tbg) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    tb = tbg - prefix[lo];
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+template <int MODE, int BNT>
+__global__ void __launch_bounds__(kThreads, 1)
+ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+              const __grid_constant__ CUtensorMap map_b1, const Params p) {
+    using C = Cfg<MODE, BNT>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int32_t prefix[kMaxExperts + 1];
+    __shared__ int32_t warp_sums[8];
+    __shared__ __align__(8) uint64_t full_bar[C::stages], empty_bar[C::stages];
+    __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t smem_base = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::stages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull_bar[b]), 1);
+            mbar_init(smem_u32(&tempty_bar[b]), 4);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b0);
+        if (C::glu) tma_prefetch_desc(&map_b1);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(&tmem_base_slot), C::tmem_cols);
+        tmem_relinquish();
+    }
+    build_prefix(p.offsets, p.N, C::tok_block, prefix, warp_sums);  // contains __syncthreads
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_slot;
+
+    const int nfb = (p.out_dim + C::feat_block - 1) / C::feat_block;
+    const int total_tiles = prefix[p.N] * nfb;
+    const int kblocks = (p.kdim + kBK - 1) / kBK;
+    volatile int *abort_v = &abort_flag;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (one thread)
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                int e, tb, fb;
+                tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
+                const int tok0 = p.offsets[e] + tb * C::tok_block;
+                const int f0 = fb * C::feat_block;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % C::stages;
+                    const uint32_t ph = (it / C::stages) & 1;
+                    if (!wait_bar(smem_u32(&empty_bar[s]), ph ^ 1, abort_v, p.status)) { ok = false; break; }
+                    const uint32_t fb_ = smem_u32(&full_bar[s]);
+                    const uint32_t sa = smem_base + s * C::stage_bytes;
+                    const uint32_t sb = sa + C::a_tiles * C::a_bytes;
+                    mbar_arrive_expect_tx(fb_, C::stage_bytes);
+                    const int k0 = kb * kBK;
+                    if constexpr (!C::swap) {
+                        tma_load_2d(sa, &map_a, fb_, k0, tok0);                          // token rows
+                        if constexpr (C::glu) {
+                            tma_load_3d(sb, &map_b0, fb_, k0, f0, e);                    // W_gate rows
+                            tma_load_3d(sb + 128 * 128, &map_b1, fb_, k0, f0, e);        // W_up rows
+                        } else {
+                            tma_load_3d(sb, &map_b0, fb_, k0, f0, e);                    // W_down rows
+                        }
+                    } else {
+                        tma_load_3d(sa, &map_b0, fb_, k0, f0, e);                        // W_gate / W_down
+                        if (C::glu) tma_load_3d(sa + C::a_bytes, &map_b1, fb_, k0, f0, e); // W_up
+                        tma_load_2d(sb, &map_a, fb_, k0, tok0);                          // token rows
+                    }
+                }
+            }
+            // drain: the last fill of every stage must have landed before the CTA may exit
+            for (uint32_t j = (it > (uint32_t)C::stages ? it - C::stages : 0); j < it; ++j)
+                drain_wait(smem_u32(&full_bar[j % C::stages]), (j / C::stages) & 1, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (one thread)
+        if (lane == 0) {
+            uint32_t it = 0, local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t use = local >> 1;
+                if (!wait_bar(smem_u32(&tempty_bar[acc]), (use & 1) ^ 1, abort_v, p.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * C::acc_cols;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % C::stages;
+                    const uint32_t ph = (it / C::stages) & 1;
+                    if (!wait_bar(smem_u32(&full_bar[s]), ph, abort_v, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_base + s * C::stage_bytes;
+                    const uint32_t sb = sa + C::a_tiles * C::a_bytes;
+#pragma unroll
+                    for (int j = 0; j < kBK / 16; ++j) {
+                        const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+                        const uint64_t bdesc = smem_desc_sw128(sb + j * 32);
+                        mma_bf16(d_tmem, smem_desc_sw128(sa + j * 32), bdesc, C::idesc, accum);
+                        if (C::swap && C::glu)
+                            mma_bf16(d_tmem + BNT, smem_desc_sw128(sa + C::a_bytes + j * 32), bdesc, C::idesc,
+                                     accum);
+                    }
+                    mma_commit(smem_u32(&empty_bar[s]));  // frees the stage once these MMAs are done
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&tfull_bar[acc]));      // accumulator ready for the epilogue
+            }
+            // drain: no MMA may be in flight when TMEM is freed
+            mma_commit(smem_u32(&drain_bar));
+            drain_wait(smem_u32(&drain_bar), 0, p.status);
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+        // ------------------------------------------------ epilogue (warps 4..7)
+        const int q = warp & 3;                    // TMEM lane quarter
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        uint32_t local = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t use = local >> 1;
+            bool ok = wait_bar(smem_u32(&tfull_bar[acc]), use & 1, abort_v, p.status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            int e, tb, fb;
+            tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
+            const int cnt = p.offsets[e + 1] - p.offsets[e];
+            const int tok0 = p.offsets[e] + tb * C::tok_block;
+            const int ntok = min(C::tok_block, cnt - tb * C::tok_block);  // valid token rows of this tile
+            const int f0 = fb * C::feat_block;
+            const uint32_t t_acc = tmem_base + acc * C::acc_cols + lane_addr;
+            if constexpr (!C::swap) {
+                // thread = token row r; columns = output features
+                const int r = q * 32 + lane;
+                const bool row_ok = r < ntok;
+                __nv_bfloat16 *orow = p.out + (int64_t)(tok0 + r) * p.out_dim;
+                constexpr int chunks = C::glu ? 4 : 8;  // 32-column chunks of output
+#pragma unroll 1
+                for (int c = 0; c < chunks; ++c) {
+                    uint32_t va[32];
+                    float o[32];
+                    tmem_ld_x32(t_acc + c * 32, va);
+                    if constexpr (C::glu) {
+                        uint32_t vu[32];
+                        tmem_ld_x32(t_acc + 128 + c * 32, vu);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            o[j] = swiglu_fast(__uint_as_float(va[j]), __uint_as_float(vu[j]));
+                    } else {
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(va[j]);
+                    }
+                    const int col0 = f0 + c * 32;
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = col0 + v * 8;
+                            if (col < p.out_dim) {  // out_dim is a multiple of 8
+                                uint4 pk;
+                                pk.x = pack_bf16x2(o[v * 8 + 0], o[v * 8 + 1]);
+                                pk.y = pack_bf16x2(o[v * 8 + 2], o[v * 8 + 3]);
+                                pk.z = pack_bf16x2(o[v * 8 + 4], o[v * 8 + 5]);
+                                pk.w = pack_bf16x2(o[v * 8 + 6], o[v * 8 + 7]);
+                                *reinterpret_cast<uint4 *>(orow + col) = pk;
+                            }
+                        }
+                    }
+                }
+            } else {
+                // thread = output feature f; columns = token rows of the tile
+                const int f = f0 + q * 32 + lane;
+                const bool f_ok = f < p.out_dim;
+                constexpr int CH = BNT < 32 ? (BNT > 0 ? BNT : 16) : 32;
+#pragma unroll 1
+                for (int c = 0; c < C::tok_block / CH; ++c) {
+                    float o[CH];
+                    if constexpr (CH == 32) {
+                        uint32_t va[32];
+                        tmem_ld_x32(t_acc + c * 32, va);
+                        if constexpr (C::glu) {
+                            uint32_t vu[32];
+                            tmem_ld_x32(t_acc + BNT + c * 32, vu);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < CH; ++j)
+                                o[j] = swiglu_fast(__uint_as_float(va[j]), __uint_as_float(vu[j]));
+                        } else {
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < CH; ++j) o[j] = __uint_as_float(va[j]);
+                        }
+                    } else {
+                        uint32_t va[16];
+                        tmem_ld_x16(t_acc + c * 16, va);
+                        if constexpr (C::glu) {
+                            uint32_t vu[16];
+                            tmem_ld_x16(t_acc + BNT + c * 16, vu);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < CH; ++j)
+                                o[j] = swiglu_fast(__uint_as_float(va[j]), __uint_as_float(vu[j]));
+                        } else {
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < CH; ++j) o[j] = __uint_as_float(va[j]);
+                        }
+                    }
+                    if (f_ok) {
+#pragma unroll
+                        for (int j = 0; j < CH; ++j) {
+                            const int t = c * CH + j;
+                            if (t < ntok) p.out[(int64_t)(tok0 + t) * p.out_dim + f] = __float2bfloat16_rn(o[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem_base, C::tmem_cols);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side: tensor maps and launches
+// ---------------------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2D row-major [rows, cols] bf16, box {64, box_rows}, 128-byte swizzle.
+bool make_map_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D row-major [n, rows, cols] bf16 (one matrix per expert), box {64, box_rows, 1}.
+bool make_map_3d(CUtensorMap *m, const void *base, int64_t n, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)n};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(cols * rows * 2)};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+template <int MODE, int BNT>
+cudaError_t launch_mode(const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1, const Params &p,
+                        int64_t tile_bound, cudaStream_t s) {
+    using C = Cfg<MODE, BNT>;
+    auto kern = ffn_tc_kernel<MODE, BNT>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes);
+    if (err != cudaSuccess) return err;
+    const int grid = (int)std::min<int64_t>(tile_bound, (int64_t)sm_count());
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, kThreads, C::smem_bytes, s>>>(ma, mb0, mb1, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <int BNT>
+cudaError_t launch_swap(const void *x_perm, const int32_t *offsets, int64_t N, int64_t P, int64_t d, int64_t I,
+                        const void *wg, const void *wu, const void *wd, void *h, void *y_perm, uint32_t *status,
+                        cudaStream_t s) {
+    CUtensorMap mx, mh, mg, mu, mdn;
+    if (!make_map_2d(&mx, x_perm, P, d, BNT) || !make_map_2d(&mh, h, P, I, BNT) ||
+        !make_map_3d(&mg, wg, N, I, d, kBM) || !make_map_3d(&mu, wu, N, I, d, kBM) ||
+        !make_map_3d(&mdn, wd, N, d, I, kBM))
+        return cudaErrorInvalidValue;
+    const int64_t tok_blocks = cdiv(P, BNT) + N;
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status};
+    cudaError_t err = launch_mode<SWAP_GLU, BNT>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s);
+    if (err != cudaSuccess) return err;
+    mark_stage(MOGE_STAGE_DOWN, s);
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status};
+    return launch_mode<SWAP_PLAIN, BNT>(mh, mdn, mdn, p2, tok_blocks * cdiv(d, 128), s);
+}
+
+}  // namespace tc
+
+cudaError_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, int64_t N, int64_t P, int64_t T, int64_t d,
+                          int64_t I, const void *w_gate, const void *w_up, const void *w_down, void *h,
+                          void *y_perm, uint32_t *status, cudaStream_t s) {
+    using namespace tc;
+    if (P == 0) return cudaSuccess;
+    if (N > kMaxExperts) return cudaErrorInvalidValue;
+    // A token selects an expert at most once, so no expert has more than T rows: with T <= 64
+    // every expert fits one weights-as-M tile column.
+    if (T <= 16) return launch_swap<16>(x_perm, offsets, N, P, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
+    if (T <= 32) return launch_swap<32>(x_perm, offsets, N, P, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
+    if (T <= 64) return launch_swap<64>(x_perm, offsets, N, P, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
+    CUtensorMap mx, mh, mg, mu, mdn;
+    if (!make_map_2d(&mx, x_perm, P, d, kBM) || !make_map_2d(&mh, h, P, I, kBM) ||
+        !make_map_3d(&mg, w_gate, N, I, d, 128) || !make_map_3d(&mu, w_up, N, I, d, 128) ||
+        !make_map_3d(&mdn, w_down, N, d, I, 256))
+        return cudaErrorInvalidValue;
+    const int64_t row_blocks = cdiv(P, kBM) + N;
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status};
+    cudaError_t err = launch_mode<NORMAL_GLU, 0>(mx, mg, mu, p1, row_blocks * cdiv(I, 128), s);
+    if (err != cudaSuccess) return err;
+    mark_stage(MOGE_STAGE_DOWN, s);
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status};
+    return launch_mode<NORMAL_PLAIN, 0>(mh, mdn, mdn, p2, row_blocks * cdiv(d, 256), s);
 }
 
 }  // namespace moge
