@@ -314,6 +314,8 @@ def run_ours(args):
     pk, peak_kind = peaks()
 
     wp = WORKLOADS[args.workload]
+    if args.tokens:  # a smaller token count of the same layer (profiling captures)
+        wp = wp.with_(name=f"{wp.name}[T={args.tokens}]", T=args.tokens)
     wd = WORKLOADS["decode_t32"]
     inp = synth.layer_inputs(wp, seed=DEFAULT_SEED)   # decode reuses the same weights and the first 32 tokens
     d_inp = upload(inp, device)
@@ -329,12 +331,23 @@ def run_ours(args):
     score = float(prefill.aux["score"][0].item())
 
     # decode shape, same weights
-    dec = Layer(wd, d_inp, device)
-    dms, dstages, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist)
-    dcounts = dec.aux["counts"].cpu().numpy()
+    decode = None
+    if args.decode_steps > 0:
+        dec = Layer(wd, d_inp, device)
+        dms, dstages, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist)
+        dcounts = dec.aux["counts"].cpu().numpy()
+        decode = {"workload": wd.name, "value": round(wd.T * ws_n / (dms / 1e3), 1), "unit": "tokens/s",
+                  "ms_per_step": round(dms, 4), "steps": args.decode_steps,
+                  "roofline": gate_up_roofline(wd, dcounts, dstages["gate_up"], pk, peak_kind),
+                  "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
+                  "stage_ms": {k: round(v, 5) for k, v in dstages.items()}, "gpu_launches": int(dlaunches)}
 
     # end to end through the public call with host buffers
-    e2e_ms, h2d, d2h = e2e_steps(prefill, max(3, args.steps // 2), dist)
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_steps(prefill, max(3, args.steps // 2), dist)
+        e2e = {"value": round(wp.T * ws_n / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
     tok = wp.T * ws_n
     res = {
@@ -359,14 +372,9 @@ def run_ours(args):
         "stage_ms": {k: round(v, 5) for k, v in stages.items()},
         "imbalance_score": score,
         "clocks": clocks,
-        "e2e": {"value": round(tok / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "e2e": e2e,
         "gpu_launches": int(launches),
-        "decode": {"workload": wd.name, "value": round(wd.T * ws_n / (dms / 1e3), 1), "unit": "tokens/s",
-                   "ms_per_step": round(dms, 4), "steps": args.decode_steps,
-                   "roofline": gate_up_roofline(wd, dcounts, dstages["gate_up"], pk, peak_kind),
-                   "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
-                   "stage_ms": {k: round(v, 5) for k, v in dstages.items()}, "gpu_launches": int(dlaunches)},
+        "decode": decode,
     }
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wp, inp, budget_s=args.cpu_budget)
@@ -430,6 +438,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=300)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_t8192", choices=["prefill_t8192"])
+    ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle FFN work")
     ap.add_argument("--ref-tokens", type=int, default=8, help="FFN tokens per reference-arm step")
