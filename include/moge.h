@@ -145,6 +145,29 @@ moge_status_t moge_permute(const moge_config_t *cfg, const int32_t *topk_idx, co
                            int32_t *counts, int32_t *offsets, int32_t *pair_row, int32_t *row_token,
                            void *x_perm, void *ws, size_t ws_bytes, moge_stream_t stream);
 
+/* moge_permute without a workspace.  The paper has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory (a serving
+ * runtime whose pool already owns all of HBM and hands a plugin only its input
+ * and output buffers, or a latency-critical loop that must not call cudaMalloc,
+ * which can synchronise the device).  Arguments, outputs and errors are those
+ * of moge_permute minus ws/ws_bytes.
+ *   Scratch: a static device array of 256 KiB inside the library (held by every
+ *   GPU that loads it until the process exits), enough for
+ *   ceil(T/256) * N <= 65536 (e.g. T <= 16384 with N <= 256); larger problems
+ *   return MOGE_ERR_UNSUPPORTED before anything is launched.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   All calls share the array and it keeps the last call's contents (nothing in
+ *   it needs to start at zero): calls that overlap on the GPU race, so order
+ *   them on one stream or synchronise between them.
+ *   This call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ *   routine).  An out-of-range expert id is skipped (its pair_row is -1) but,
+ *   having no workspace, is not reported through a status word. */
+moge_status_t moge_permute_noalloc(const moge_config_t *cfg, const int32_t *topk_idx, const void *x,
+                                   int32_t *counts, int32_t *offsets, int32_t *pair_row, int32_t *row_token,
+                                   void *x_perm, moge_stream_t stream);
+
 /* Grouped expert FFN over the permuted rows (SwiGLU; bf16 on tcgen05 tensor
  * cores with TMEM accumulators, fp32 on CUDA cores).  For every expert e and
  * row r in [offsets[e], offsets[e+1]):

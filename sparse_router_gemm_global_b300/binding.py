@@ -72,6 +72,8 @@ def load():
         lib.moge_combine.argtypes = [cfgp, vp, vp, vp, vp, vp]
         lib.moge_imbalance_score.argtypes = [cfgp, vp, vp, vp, vp]
         lib.moge_layer_forward.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Aux), vp, sz, vp]
+        lib.moge_permute_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.moge_permute_noalloc.restype = i32
         lib.moge_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         lib.moge_kernel_launch_count.restype = ctypes.c_uint64
         for fn in ("moge_set_stage_events", "moge_reset_device_status", "moge_query_device_status", "moge_route", "moge_permute",
@@ -150,6 +152,13 @@ def moge_permute(cfg, topk_idx, x, counts, offsets, pair_row, row_token, x_perm,
     _check("moge_permute", load().moge_permute(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts),
                                                _ptr(offsets), _ptr(pair_row), _ptr(row_token), _ptr(x_perm),
                                                _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moge_permute_noalloc(cfg, topk_idx, x, counts, offsets, pair_row, row_token, x_perm, stream=None) -> None:
+    """moge_permute for callers that cannot hand over a workspace (scratch is a static device array)."""
+    _check("moge_permute_noalloc", load().moge_permute_noalloc(
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(pair_row), _ptr(row_token),
+        _ptr(x_perm), _stream(stream)))
 
 
 def moge_expert_ffn(cfg, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, stream=None) -> None:
