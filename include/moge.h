@@ -98,11 +98,13 @@ const char *moge_status_string(moge_status_t s);
 
 /* Bytes of scratch needed by every call below for this configuration
  * (0 when cfg is invalid).  One workspace may serve all calls of a layer in
- * stream order.  The first 256 bytes hold the device status word, which
- * must be zero before first use (see moge_reset_device_status). */
+ * stream order (calls on different streams need different workspaces).  The
+ * first 4096 bytes (the status page) hold the device status word and
+ * self-resetting per-tile counters of the router; they must be zero before
+ * first use (see moge_reset_device_status). */
 size_t moge_workspace_bytes(const moge_config_t *cfg);
 
-/* Zero the device status word at the start of ws (enqueued on stream). */
+/* Zero the 4096-byte status page at the start of ws (enqueued on stream). */
 moge_status_t moge_reset_device_status(void *ws, moge_stream_t stream);
 
 /* Synchronise `stream`, then read the status word at the start of ws:

@@ -128,7 +128,7 @@ def alloc_workspace(cfg: Config, device="cuda"):
     if n == 0:
         raise MoGEError("moge_workspace_bytes", 1)
     ws = torch.empty(n, dtype=torch.uint8, device=device)
-    ws[:256].zero_()
+    ws[:4096].zero_()  # status word + self-resetting router counters
     return ws
 
 

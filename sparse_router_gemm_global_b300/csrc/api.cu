@@ -74,6 +74,11 @@ moge_status_t route_impl(const moge_config_t *c, moge_route_mode_t mode, const v
                          cudaStream_t st) {
     const WsLayout L = ws_layout(*c);
     const float *scores = logits;
+    const bool global = mode == MOGE_ROUTE_GLOBAL_TOPK;
+    if (x && c->act_dtype == MOGE_BF16 && c->N <= 256)  // scores, softmax and selection in one launch
+        return cuda_status(launch_router_tc(x, w_router, bias, c->T, c->d, c->N, c->M, c->k_per_group, global,
+                                            logits, idx, gate, at<float>(ws, L.router_partials),
+                                            at<uint32_t>(ws, kTicketOffset), at<uint32_t>(ws, L.status), st));
     if (x) {
         float *dst = logits ? logits : at<float>(ws, L.logits);
         cudaError_t e = launch_router_logits_simt(x, w_router, bias, c->T, c->d, c->N, c->act_dtype, dst, st);
@@ -125,7 +130,7 @@ size_t moge_workspace_bytes(const moge_config_t *cfg) {
 
 moge_status_t moge_reset_device_status(void *ws, moge_stream_t stream) {
     if (!ws) return MOGE_ERR_INVALID_ARGUMENT;
-    return cuda_status(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
+    return cuda_status(cudaMemsetAsync(ws, 0, kStatusPageBytes, (cudaStream_t)stream));
 }
 
 moge_status_t moge_query_device_status(const void *ws, moge_stream_t stream) {
@@ -231,13 +236,8 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
         if (a.counts || a.offsets || a.score || a.group_load) {
             int32_t *counts = a.counts ? a.counts : at<int32_t>(ws, L.counts);
             int32_t *offsets = a.offsets ? a.offsets : at<int32_t>(ws, L.offsets);
-            cudaError_t e = launch_permute(nullptr, 0, K, cfg->N, counts, offsets, nullptr, nullptr, nullptr,
-                                           nullptr, st);
-            if (e == cudaSuccess && (a.score || a.group_load)) {
-                float *score = a.score ? a.score : at<float>(ws, L.status + 16);
-                e = launch_imbalance(counts, 0, cfg->N, cfg->M, a.group_load, score, st);
-            }
-            return cuda_status(e);
+            return cuda_status(launch_permute(nullptr, 0, K, cfg->N, counts, offsets, nullptr, nullptr, nullptr,
+                                              nullptr, st, cfg->M, a.group_load, a.score));
         }
         return MOGE_OK;
     }
@@ -253,9 +253,10 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
     mark_stage(MOGE_STAGE_ROUTE, st);
     if ((s = route_impl(cfg, MOGE_ROUTE_GROUPED, x, w_router, bias, a.logits, idx, gate, ws, st)) != MOGE_OK)
         return s;
-    mark_stage(MOGE_STAGE_PERMUTE, st);
+    mark_stage(MOGE_STAGE_PERMUTE, st);  // the permutation also writes the imbalance outputs
     cudaError_t e = launch_permute(idx, cfg->T, K, cfg->N, counts, offsets, pair_row, row_token,
-                                   at<int32_t>(ws, L.chunk_counts), at<uint32_t>(ws, L.status), st);
+                                   at<int32_t>(ws, L.chunk_counts), at<uint32_t>(ws, L.status), st, cfg->M,
+                                   a.group_load, a.score);
     mark_stage(MOGE_STAGE_GATHER, st);
     if (e == cudaSuccess)
         e = launch_gather_rows(x, row_token, offsets, cfg->N, P, cfg->d, cfg->act_dtype, x_perm, st);
@@ -264,11 +265,7 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
     if ((s = ffn_impl(cfg, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, st)) != MOGE_OK) return s;
     mark_stage(MOGE_STAGE_COMBINE, st);
     e = launch_combine(y_perm, pair_row, gate, cfg->T, K, cfg->d, cfg->act_dtype, y, st);
-    mark_stage(MOGE_STAGE_IMBALANCE, st);
-    if (e == cudaSuccess && (a.score || a.group_load)) {
-        float *score = a.score ? a.score : at<float>(ws, L.status + 16);
-        e = launch_imbalance(counts, cfg->T, cfg->N, cfg->M, a.group_load, score, st);
-    }
+    mark_stage(MOGE_STAGE_IMBALANCE, st);  // empty: computed with the permutation
     mark_stage(MOGE_NUM_STAGES, st);
     return cuda_status(e);
 }

@@ -45,11 +45,32 @@ __device__ __forceinline__ float swiglu_precise(float a, float u) { return a / (
 // Workspace layout (every region 256-byte aligned).  Computed identically on every call.
 // ---------------------------------------------------------------------------------------------
 struct WsLayout {
-    size_t status, logits, idx, gate, counts, offsets, pair_row, row_token, chunk_counts, sched,
+    size_t status, logits, idx, gate, counts, offsets, pair_row, row_token, chunk_counts, router_partials,
         x_perm, h, y_perm, total;
 };
 
 constexpr int kPermuteChunk = 256;   // tokens per permutation block
+
+// The first kStatusPageBytes of the workspace must be zero before first use: the status word
+// sits at byte 0 and self-resetting per-tile counters of the router at kTicketOffset.
+constexpr int kStatusPageBytes = 4096;
+constexpr int kTicketOffset = 256;
+constexpr int kMaxTicketTiles = (kStatusPageBytes - kTicketOffset) / 4;
+constexpr int kRouterTileRows = 128;
+constexpr int kDesignSMs = 148;  // B300 SM count: sizes the router's split of the reduction
+
+// Number of slices the tensor-core router splits its reduction over d into, so that small
+// batches still spread over more SMs (1 = no split).  At most 4 slices (each at least 16
+// k-blocks of 64): the slices are added in order by the tile's last CTA, whose latency grows
+// with their number.  Deterministic in (T, d, N).
+inline int router_kslices(int64_t T, int64_t d, int64_t N) {
+    const int64_t mtiles = cdiv(T, kRouterTileRows), kblocks = cdiv(d, 64);
+    if (T <= 0 || mtiles > kMaxTicketTiles || N % 4 != 0) return 1;
+    int64_t s = kDesignSMs / mtiles;
+    if (s > kblocks / 16) s = kblocks / 16;
+    if (s > 4) s = 4;
+    return s < 1 ? 1 : (int)s;
+}
 
 inline WsLayout ws_layout(const moge_config_t &c) {
     const int64_t K = c.M * c.k_per_group;
@@ -59,7 +80,7 @@ inline WsLayout ws_layout(const moge_config_t &c) {
     WsLayout L{};
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off += (size_t)round_up((int64_t)bytes, 256); return o; };
-    L.status = take(256);
+    L.status = take(kStatusPageBytes);
     L.logits = take((size_t)c.T * c.N * 4);
     L.idx = take((size_t)P * 4);
     L.gate = take((size_t)P * 4);
@@ -68,7 +89,10 @@ inline WsLayout ws_layout(const moge_config_t &c) {
     L.pair_row = take((size_t)P * 4);
     L.row_token = take((size_t)P * 4);
     L.chunk_counts = take((size_t)chunks * c.N * 4);
-    L.sched = take(64 * 1024);
+    {
+        const int s = router_kslices(c.T, c.d, c.N);
+        L.router_partials = take(s > 1 ? (size_t)cdiv(c.T, kRouterTileRows) * s * kRouterTileRows * c.N * 4 : 0);
+    }
     L.x_perm = take((size_t)P * c.d * es);
     L.h = take((size_t)P * c.I * es);
     L.y_perm = take((size_t)P * c.d * es);
@@ -81,11 +105,19 @@ inline WsLayout ws_layout(const moge_config_t &c) {
 // ---------------------------------------------------------------------------------------------
 cudaError_t launch_route_select(const float *logits, int64_t T, int64_t N, int64_t M, int64_t kpg,
                                 bool global, int32_t *idx, float *gate, cudaStream_t s);
+// cuTensorMapEncodeTiled from the driver (nullptr if unavailable); defined in ffn_tc.cu.
+void *tensor_map_encoder();
+
+// Fused tensor-core router (bf16, N <= 256): scores, softmax and selection in one launch.
+cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, int64_t T, int64_t d, int64_t N,
+                             int64_t M, int64_t kpg, bool global, float *logits_out, int32_t *idx, float *gate,
+                             float *partials, uint32_t *tickets, uint32_t *status, cudaStream_t s);
 cudaError_t launch_router_logits_simt(const void *x, const void *w_r, const float *bias, int64_t T,
                                       int64_t d, int64_t N, int dtype, float *logits, cudaStream_t s);
 cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, int32_t *counts,
                            int32_t *offsets, int32_t *pair_row, int32_t *row_token, int32_t *chunk_counts,
-                           uint32_t *status, cudaStream_t s);
+                           uint32_t *status, cudaStream_t s, int64_t M = 1, int32_t *group_load = nullptr,
+                           float *score = nullptr);
 cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const int32_t *offsets,
                                int64_t N, int64_t P, int64_t d, int dtype, void *x_perm, cudaStream_t s);
 cudaError_t launch_imbalance(const int32_t *counts, int64_t T, int64_t N, int64_t M, int32_t *group_load,

@@ -18,7 +18,7 @@
 // the expert's count (or past the tensor) are loaded (other experts' rows or TMA zero fill)
 // but never stored.
 //
-// Every mbarrier wait is bounded (kTimeoutNs).  A wait that gives up sets the workspace
+// Every mbarrier wait is bounded (kWaitTimeoutNs).  A wait that gives up sets the workspace
 // status word (MOGE_ERR_TIMEOUT through moge_query_device_status), raises a CTA-wide abort
 // flag that ends the other roles' loops, drains the copies and MMAs it issued and frees TMEM
 // before the CTA exits.
@@ -27,6 +27,7 @@
 
 #include "ffn_tc.cuh"
 #include "tc_ptx.cuh"
+#include "tc_wait.cuh"
 
 namespace moge {
 namespace tc {
@@ -38,7 +39,6 @@ constexpr int kBK = 64;             // k-block: 64 bf16 = 128 bytes = one 128B-s
 constexpr int kThreads = 256;       // 8 warps
 constexpr int kEpiWarp0 = 4;        // epilogue warps 4..7 (TMEM lane quarter = warp % 4)
 constexpr int kMaxExperts = 1024;
-constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kSmemBudget = 220 * 1024;
 
 enum Mode { NORMAL_GLU = 0, NORMAL_PLAIN = 1, SWAP_GLU = 2, SWAP_PLAIN = 3 };
@@ -73,35 +73,6 @@ struct Params {
     __nv_bfloat16 *out;      // [P, out_dim]
     uint32_t *status;        // workspace status word
 };
-
-// Bounded wait.  Returns false (and raises the abort flag) if it gives up.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         uint32_t *status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 31) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs || n > (1u << 30)) {
-                *abort_flag = 1;
-                raise_status(status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
-// Bounded wait that ignores the abort flag: used at exit for copies and MMAs already issued.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t *status) {
-    const uint64_t t0 = globaltimer();
-    for (uint32_t n = 0; !mbar_try_wait(bar, parity); ++n) {
-        if ((n & 31) == 31 && (globaltimer() - t0 > kTimeoutNs || n > (1u << 30))) {
-            raise_status(status, kStatusTimeout);
-            return;
-        }
-    }
-}
 
 // prefix[e] = sum over e' < e of ceil(count_e' / tok_block); all 256 threads, N <= 1024.
 __device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int tok_block, int32_t *prefix,
@@ -414,17 +385,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 // ---------------------------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
 }
 
 // 2D row-major [rows, cols] bf16, box {64, box_rows}, 128-byte swizzle.
@@ -497,6 +458,21 @@ cudaError_t launch_swap(const void *x_perm, const int32_t *offsets, int64_t N, i
 }
 
 }  // namespace tc
+
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime (no -lcuda link).
+void *tensor_map_encoder() {
+    static void *fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = ptr;
+    });
+    return fn;
+}
 
 cudaError_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, int64_t N, int64_t P, int64_t T, int64_t d,
                           int64_t I, const void *w_gate, const void *w_up, const void *w_down, void *h,

@@ -53,10 +53,35 @@ __global__ void permute_count_kernel(const int32_t *__restrict__ idx, int64_t T,
     }
 }
 
-// One block: chunk_counts -> per-chunk bases (in place), counts, offsets.
+// Optional imbalance score from per-expert counts in shared memory (the whole block calls it):
+// group_load[g] = sum of the counts of group g's experts, score = (max - min) / T (fp32).
+// `loads` is shared scratch of M ints.
+__device__ __forceinline__ void block_imbalance(const int32_t *cnt, int N, int M, int64_t T, int32_t *loads,
+                                                int32_t *__restrict__ group_load, float *__restrict__ score) {
+    if (!group_load && !score) return;
+    const int G = N / M;
+    for (int g = threadIdx.x; g < M; g += blockDim.x) {
+        int s = 0;
+        for (int e = g * G; e < (g + 1) * G; ++e) s += cnt[e];
+        loads[g] = s;
+        if (group_load) group_load[g] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && score) {
+        int mx = loads[0], mn = loads[0];
+        for (int g = 1; g < M; ++g) {
+            mx = max(mx, loads[g]);
+            mn = min(mn, loads[g]);
+        }
+        *score = T > 0 ? (float)(mx - mn) / (float)T : 0.f;
+    }
+}
+
+// One block: chunk_counts -> per-chunk bases (in place), counts, offsets (+ imbalance).
 __global__ void permute_scan_kernel(int32_t *__restrict__ chunk_counts, int chunks, int N,
-                                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets) {
-    extern __shared__ int32_t tot[];  // [N]
+                                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int M,
+                                    int64_t T, int32_t *__restrict__ group_load, float *__restrict__ score) {
+    extern __shared__ int32_t tot[];  // [N] counts, then [M] group loads
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
         int run = 0;
         for (int c = 0; c < chunks; ++c) {
@@ -76,6 +101,7 @@ __global__ void permute_scan_kernel(int32_t *__restrict__ chunk_counts, int chun
         }
         offsets[N] = run;
     }
+    block_imbalance(tot, N, M, T, tot + N, group_load, score);
 }
 
 // Rows of the chunk's pairs.  base[e] = offsets[e] + bases of earlier chunks.
@@ -120,15 +146,17 @@ __global__ void permute_scatter_kernel(const int32_t *__restrict__ idx, int64_t 
     scatter_rows(idx, T, K, N, masks, warp_base, base, pair_row, row_token);
 }
 
-// T <= kChunk: count, scan and scatter in one block.
+// T <= kChunk: count, scan and scatter in one block (+ imbalance).
 __global__ void permute_single_kernel(const int32_t *__restrict__ idx, int64_t T, int K, int N,
                                       int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                                       int32_t *__restrict__ pair_row, int32_t *__restrict__ row_token,
-                                      uint32_t *status) {
+                                      uint32_t *status, int M, int32_t *__restrict__ group_load,
+                                      float *__restrict__ score) {
     extern __shared__ uint32_t sm[];
     uint32_t *masks = sm;
     int32_t *warp_base = (int32_t *)(sm + kWarps * N);
     int32_t *base = warp_base + kWarps * N;
+    int32_t *loads = base + N;
     build_masks(idx, T, K, N, masks, status);
     __syncthreads();
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
@@ -136,6 +164,8 @@ __global__ void permute_single_kernel(const int32_t *__restrict__ idx, int64_t T
         for (int w = 0; w < kWarps; ++w) c += __popc(masks[w * N + e]);
         base[e] = c;
     }
+    __syncthreads();
+    block_imbalance(base, N, M, T, loads, group_load, score);
     __syncthreads();
     if (threadIdx.x == 0) {
         int run = 0;
@@ -152,29 +182,34 @@ __global__ void permute_single_kernel(const int32_t *__restrict__ idx, int64_t T
     scatter_rows(idx, T, K, N, masks, warp_base, base, pair_row, row_token);
 }
 
-__global__ void zero_counts_kernel(int N, int32_t *counts, int32_t *offsets) {
+__global__ void zero_counts_kernel(int N, int32_t *counts, int32_t *offsets, int M, int32_t *group_load,
+                                   float *score) {
     for (int e = threadIdx.x; e <= N; e += blockDim.x) {
         if (e < N) counts[e] = 0;
         offsets[e] = 0;
     }
+    if (group_load)
+        for (int g = threadIdx.x; g < M; g += blockDim.x) group_load[g] = 0;
+    if (score && threadIdx.x == 0) *score = 0.f;
 }
 
 cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, int32_t *counts,
                            int32_t *offsets, int32_t *pair_row, int32_t *row_token, int32_t *chunk_counts,
-                           uint32_t *status, cudaStream_t s) {
+                           uint32_t *status, cudaStream_t s, int64_t M, int32_t *group_load, float *score) {
     if (T == 0) {
-        zero_counts_kernel<<<1, 256, 0, s>>>((int)N, counts, offsets);
+        zero_counts_kernel<<<1, 256, 0, s>>>((int)N, counts, offsets, (int)M, group_load, score);
         count_launches(1);
         return cudaGetLastError();
     }
-    const size_t smem_scatter = (size_t)(2 * kWarps * N + N) * 4;
+    const size_t smem_scatter = (size_t)(2 * kWarps * N + N + M) * 4;
     cudaError_t err;
     if (T <= kChunk) {
         err = cudaFuncSetAttribute(permute_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem_scatter);
         if (err != cudaSuccess) return err;
         permute_single_kernel<<<1, kChunk, smem_scatter, s>>>(idx, T, (int)K, (int)N, counts, offsets,
-                                                              pair_row, row_token, status);
+                                                              pair_row, row_token, status, (int)M, group_load,
+                                                              score);
         count_launches(1);
         return cudaGetLastError();
     }
@@ -188,7 +223,8 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
     if (err != cudaSuccess) return err;
     permute_count_kernel<<<chunks, kChunk, smem_count, s>>>(idx, T, (int)K, (int)N, chunk_counts, status);
     count_launches(1);
-    permute_scan_kernel<<<1, 1024, (size_t)N * 4, s>>>(chunk_counts, chunks, (int)N, counts, offsets);
+    permute_scan_kernel<<<1, 1024, (size_t)(N + M) * 4, s>>>(chunk_counts, chunks, (int)N, counts, offsets,
+                                                             (int)M, T, group_load, score);
     count_launches(1);
     permute_scatter_kernel<<<chunks, kChunk, smem_scatter, s>>>(idx, T, (int)K, (int)N, chunk_counts,
                                                                 offsets, pair_row, row_token);
@@ -197,12 +233,14 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
 }
 
 // ---------------------------------------------------------------------------------------------
-// Row gather x_perm[r,:] = x[row_token[r],:]; one warp per row, 16-byte vectors.
+// Row gather x_perm[r,:] = x[row_token[r],:]; one warp per row, 16-byte vectors, each lane
+// issuing 8 loads before their stores so that a row's reads are in flight together.
 // Only rows r < offsets[N] (the pairs that exist) are copied.
 // ---------------------------------------------------------------------------------------------
 __global__ void gather_rows_kernel(const int4 *__restrict__ x, const int32_t *__restrict__ row_token,
                                    const int32_t *__restrict__ offsets, int N, int64_t vec_per_row,
                                    int4 *__restrict__ x_perm) {
+    constexpr int kBatch = 8;
     const int64_t rows = offsets[N];
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -211,7 +249,19 @@ __global__ void gather_rows_kernel(const int4 *__restrict__ x, const int32_t *__
         const int64_t t = row_token[r];
         const int4 *src = x + t * vec_per_row;
         int4 *dst = x_perm + r * vec_per_row;
-        for (int64_t v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+        for (int64_t v0 = lane; v0 < vec_per_row; v0 += 32 * kBatch) {
+            int4 buf[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int64_t v = v0 + 32 * j;
+                if (v < vec_per_row) buf[j] = __ldg(src + v);
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int64_t v = v0 + 32 * j;
+                if (v < vec_per_row) dst[v] = buf[j];
+            }
+        }
     }
 }
 

@@ -8,44 +8,9 @@
 // index, so it is independent of how exp() rounds; the gates are
 // exp(l - max) / sum_e exp(l_e - max) with a compensated fp32 sum.
 #include "common.cuh"
+#include "route_token.cuh"
 
 namespace moge {
-
-// Route one token from its scores l[0..N).  groups/G/per describe the
-// selection: GROUPED = (M, N/M, K'), GLOBAL = (1, N, M*K').
-__device__ __forceinline__ void route_token(const float *l, int N, int groups, int G, int per,
-                                            int32_t *idx_out, float *gate_out) {
-    float m = l[0];
-    for (int e = 1; e < N; ++e) m = fmaxf(m, l[e]);
-    // Neumaier-compensated sum of exp(l - m)
-    float s = 0.f, comp = 0.f;
-    for (int e = 0; e < N; ++e) {
-        const float v = expf(l[e] - m);
-        const float t = s + v;
-        comp += (fabsf(s) >= fabsf(v)) ? ((s - t) + v) : ((v - t) + s);
-        s = t;
-    }
-    s += comp;
-    for (int g = 0; g < groups; ++g) {
-        // walk the group's experts in rank order: each round takes the best
-        // expert ranking strictly after the previously taken one
-        float last_v = __int_as_float(0x7f800000);  // +inf
-        int last_e = -1;
-        for (int r = 0; r < per; ++r) {
-            float bv = 0.f;
-            int be = -1;
-            for (int e = g * G; e < (g + 1) * G; ++e) {
-                const float v = l[e];
-                const bool after = (v < last_v) || (v == last_v && e > last_e);
-                if (after && (be < 0 || v > bv)) { bv = v; be = e; }
-            }
-            idx_out[g * per + r] = be;
-            gate_out[g * per + r] = expf(bv - m) / s;
-            last_v = bv;
-            last_e = be;
-        }
-    }
-}
 
 __global__ void route_select_kernel(const float *__restrict__ logits, int T, int N, int groups, int G,
                                     int per, int32_t *__restrict__ idx, float *__restrict__ gate) {

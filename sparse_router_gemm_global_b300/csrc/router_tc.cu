@@ -1,0 +1,291 @@
+// Fused router on tcgen05 tensor cores: scores = x W_r^T + b (bf16 in, fp32 accumulation in
+// TMEM), then, in the same launch, the global softmax over all N experts and the top-K'
+// selection inside every group (Pangu Pro MoE explainer, section 1: scores for all experts,
+// one softmax over them, a local top-K' per group).
+//
+// One CTA per (128-token tile, slice of the reduction over d).  128 threads: thread 0 of warp 0
+// issues TMA loads, thread 0 of warp 1 issues the MMAs (M = 128 tokens, N = N rounded up to 16
+// experts), then all four warps drain TMEM (warp w owns TMEM lanes 32w..32w+31 = token rows).
+// With one slice the CTA stages its fp32 scores in shared memory and routes its tokens.  With
+// S > 1 slices (small batches, so that more SMs stream W_r) every CTA writes its partial sums
+// to the workspace; the last CTA of a tile to finish (a counter in the workspace status page,
+// reset by that CTA) adds the S partials in slice order -- so the result does not depend on
+// which CTA finishes last -- and routes the tile.  No CTA waits on another.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "route_token.cuh"
+#include "tc_ptx.cuh"
+#include "tc_wait.cuh"
+
+namespace moge {
+namespace rt {
+
+using namespace ptx;
+
+constexpr int kThreads = 128;
+constexpr int kBM = kRouterTileRows;   // tokens per tile (MMA M)
+constexpr int kBK = 64;                // bf16 elements per k-block (one 128-byte swizzle row)
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 200 * 1024;
+
+struct Params {
+    int T, d, N, npad, kblocks, kslices, kb_per_slice, stages, stage_bytes, tmem_cols;
+    int groups, G, per;
+    uint32_t idesc;
+    const float *bias;
+    float *logits;     // optional [T, N] output
+    int32_t *idx;      // [T, K]
+    float *gate;       // [T, K]
+    float *partials;   // [tiles][kslices][128][N] when kslices > 1
+    uint32_t *tickets; // [tiles] when kslices > 1
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                 const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], tfull_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ int is_last;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t smem_base = smem_u32(smem);
+    const int tile = blockIdx.x, slice = blockIdx.y;
+    const int t0 = tile * kBM;
+    const int ntok = min(kBM, p.T - t0);
+    const int kb0 = slice * p.kb_per_slice;
+    const int kb1 = min(p.kblocks, kb0 + p.kb_per_slice);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_u32(&tfull_bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&map_x);
+        tma_prefetch_desc(&map_w);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_slot), p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    volatile int *abort_v = &abort_flag;
+
+    if (warp == 0 && lane == 0) {
+        // TMA producer
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = it % p.stages;
+            const uint32_t ph = (it / p.stages) & 1;
+            if (!wait_bar(smem_u32(&empty_bar[s]), ph ^ 1, abort_v, p.status)) break;
+            const uint32_t fb = smem_u32(&full_bar[s]);
+            const uint32_t sa = smem_base + s * p.stage_bytes;
+            mbar_arrive_expect_tx(fb, p.stage_bytes);
+            tma_load_2d(sa, &map_x, fb, kb * kBK, t0);                    // 128 token rows
+            tma_load_2d(sa + kBM * 128, &map_w, fb, kb * kBK, 0);         // npad expert rows
+        }
+        for (uint32_t j = (it > (uint32_t)p.stages ? it - p.stages : 0); j < it; ++j)
+            drain_wait(smem_u32(&full_bar[j % p.stages]), (j / p.stages) & 1, p.status);
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = it % p.stages;
+            const uint32_t ph = (it / p.stages) & 1;
+            if (!wait_bar(smem_u32(&full_bar[s]), ph, abort_v, p.status)) break;
+            tc_fence_after();
+            const uint32_t sa = smem_base + s * p.stage_bytes;
+            const uint32_t sb = sa + kBM * 128;
+#pragma unroll
+            for (int j = 0; j < kBK / 16; ++j)
+                mma_bf16(tmem, smem_desc_sw128(sa + j * 32), smem_desc_sw128(sb + j * 32), p.idesc,
+                         (kb > kb0 || j > 0) ? 1u : 0u);
+            mma_commit(smem_u32(&empty_bar[s]));
+        }
+        mma_commit(smem_u32(&tfull_bar));  // also the drain: arrives once every MMA above is done
+    }
+    __syncwarp();
+
+    // ---- drain TMEM: thread = token row r of the tile
+    bool ok = wait_bar(smem_u32(&tfull_bar), 0, abort_v, p.status);
+    ok = __all_sync(0xffffffffu, ok) && !*abort_v;
+    tc_fence_after();
+    const int r = warp * 32 + lane;
+    const int stride = p.N + 1;
+    float *stage = reinterpret_cast<float *>(smem);  // [128][N+1], reuses the pipeline buffers
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    float *my_partial = p.kslices > 1
+        ? p.partials + (((size_t)tile * p.kslices + slice) * kBM + r) * p.N : nullptr;
+    for (int c0 = 0; c0 < p.npad; c0 += 16) {
+        uint32_t v[16];
+        if (ok) {
+            tmem_ld_x16(taddr + c0, v);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0u;
+        }
+        if (r < ntok) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int c = c0 + j;
+                if (c < p.N) {
+                    if (my_partial) my_partial[c] = __uint_as_float(v[j]);
+                    else stage[r * stride + c] = __uint_as_float(v[j]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
+
+    if (p.kslices > 1) {
+        // the last slice CTA of this tile sums the partials in slice order
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uint32_t ticket = atomicAdd(&p.tickets[tile], 1u);
+            is_last = (ticket == (uint32_t)p.kslices - 1);
+            if (is_last) p.tickets[tile] = 0u;  // ready for the next call
+        }
+        __syncthreads();
+        if (!is_last) return;
+        __threadfence();
+        // Each thread owns up to kRed float4 of the tile and adds the slices in order s = 0..S-1;
+        // the kRed loads of one slice are independent, so they are in flight together.
+        constexpr int kRed = 16;
+        const float4 *base = reinterpret_cast<const float4 *>(p.partials + (size_t)tile * p.kslices * kBM * p.N);
+        const int n4 = ntok * p.N / 4;  // N is a multiple of 4 on this path
+        const size_t slice4 = (size_t)kBM * p.N / 4;
+        for (int i0 = threadIdx.x; i0 < n4; i0 += kThreads * kRed) {
+            float4 acc[kRed];
+#pragma unroll
+            for (int j = 0; j < kRed; ++j) {
+                const int i = i0 + j * kThreads;
+                acc[j] = i < n4 ? __ldcg(base + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            for (int s = 1; s < p.kslices; ++s) {
+#pragma unroll
+                for (int j = 0; j < kRed; ++j) {
+                    const int i = i0 + j * kThreads;
+                    if (i < n4) {
+                        const float4 v = __ldcg(base + s * slice4 + i);
+                        acc[j].x += v.x;
+                        acc[j].y += v.y;
+                        acc[j].z += v.z;
+                        acc[j].w += v.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kRed; ++j) {
+                const int i = (i0 + j * kThreads) * 4;
+                if (i < n4 * 4) {
+                    const int rr = i / p.N, c = i - rr * p.N;  // 4 | N: the float4 stays in one row
+                    float *dst = stage + rr * stride + c;
+                    dst[0] = acc[j].x;
+                    dst[1] = acc[j].y;
+                    dst[2] = acc[j].z;
+                    dst[3] = acc[j].w;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- bias, optional scores output, softmax + selection
+    for (int i = threadIdx.x; i < ntok * p.N; i += kThreads) {
+        const int rr = i / p.N, c = i - rr * p.N;
+        float v = stage[rr * stride + c];
+        if (p.bias) v += p.bias[c];
+        stage[rr * stride + c] = v;
+        if (p.logits) p.logits[(size_t)(t0 + rr) * p.N + c] = v;
+    }
+    __syncthreads();
+    if (r < ntok) {
+        const int K = p.groups * p.per;
+        route_token(stage + r * stride, p.N, p.groups, p.G, p.per, p.idx + (size_t)(t0 + r) * K,
+                    p.gate + (size_t)(t0 + r) * K);
+    }
+}
+
+}  // namespace rt
+
+cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, int64_t T, int64_t d, int64_t N,
+                             int64_t M, int64_t kpg, bool global, float *logits_out, int32_t *idx, float *gate,
+                             float *partials, uint32_t *tickets, uint32_t *status, cudaStream_t s) {
+    using namespace rt;
+    if (T == 0) return cudaSuccess;
+    if (N > 256) return cudaErrorInvalidValue;
+    auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+    if (!fn) return cudaErrorNotSupported;
+    Params p{};
+    p.T = (int)T;
+    p.d = (int)d;
+    p.N = (int)N;
+    p.npad = (int)round_up(N, 16);
+    p.kblocks = (int)cdiv(d, kBK);
+    p.kslices = router_kslices(T, d, N);
+    p.kb_per_slice = (int)cdiv(p.kblocks, p.kslices);
+    p.kslices = (int)cdiv(p.kblocks, p.kb_per_slice);  // no empty slice
+    p.stage_bytes = kBM * 128 + p.npad * 128;
+    p.stages = std::min(kMaxStages, kSmemBudget / p.stage_bytes);
+    int cols = 32;
+    while (cols < p.npad) cols <<= 1;
+    p.tmem_cols = cols;
+    p.groups = global ? 1 : (int)M;
+    p.G = global ? (int)N : (int)(N / M);
+    p.per = global ? (int)(M * kpg) : (int)kpg;
+    p.idesc = ptx::idesc_bf16_f32(kBM, p.npad);
+    p.bias = bias;
+    p.logits = logits_out;
+    p.idx = idx;
+    p.gate = gate;
+    p.partials = partials;
+    p.tickets = tickets;
+    p.status = status;
+    const size_t stage_floats = (size_t)kBM * (N + 1) * 4;
+    size_t smem = std::max((size_t)p.stages * p.stage_bytes, stage_floats) + 1024;
+
+    CUtensorMap mx, mw;
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)T};
+        cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+        cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+        cuuint32_t estr[2] = {1, 1};
+        if (fn(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+        cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)p.npad};
+        cuuint32_t estr[2] = {1, 1};
+        if (fn(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w_r), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)cdiv(T, kBM), (unsigned)p.kslices);
+    router_tc_kernel<<<grid, kThreads, smem, s>>>(mx, mw, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moge
