@@ -89,15 +89,17 @@ moge_status_t route_impl(const moge_config_t *c, moge_route_mode_t mode, const v
                                            mode == MOGE_ROUTE_GLOBAL_TOPK, idx, gate, st));
 }
 
-moge_status_t ffn_impl(const moge_config_t *c, const void *x_perm, const int32_t *offsets, const void *wg,
-                       const void *wu, const void *wd, void *y_perm, void *ws, cudaStream_t st) {
+// act = x_perm (row_token == nullptr) or x gathered through row_token (bf16 only).
+moge_status_t ffn_impl(const moge_config_t *c, const void *act, const int32_t *row_token, const int32_t *offsets,
+                       const void *wg, const void *wu, const void *wd, void *y_perm, void *ws, cudaStream_t st) {
     const WsLayout L = ws_layout(*c);
     const int64_t P = c->T * c->M * c->k_per_group;
     void *h = at<void>(ws, L.h);
     uint32_t *status = at<uint32_t>(ws, L.status);
     if (c->act_dtype == MOGE_BF16)
-        return cuda_status(launch_ffn_tc(x_perm, offsets, c->N, P, c->T, c->d, c->I, wg, wu, wd, h, y_perm,
+        return cuda_status(launch_ffn_tc(act, row_token, offsets, c->N, P, c->T, c->d, c->I, wg, wu, wd, h, y_perm,
                                          status, st));
+    const void *x_perm = act;
     return cuda_status(launch_ffn_simt(x_perm, offsets, c->N, P, c->d, c->I, c->act_dtype, wg, wu, wd, h,
                                        y_perm, st));
 }
@@ -189,7 +191,7 @@ moge_status_t moge_expert_ffn(const moge_config_t *cfg, const void *x_perm, cons
     for (const void *p : {x_perm, (const void *)offsets, w_gate, w_up, w_down, (const void *)y_perm})
         if (!aligned16(p)) return MOGE_ERR_INVALID_ARGUMENT;
     if ((s = check_ws(cfg, ws, ws_bytes)) != MOGE_OK) return s;
-    return ffn_impl(cfg, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, (cudaStream_t)stream);
+    return ffn_impl(cfg, x_perm, nullptr, offsets, w_gate, w_up, w_down, y_perm, ws, (cudaStream_t)stream);
 }
 
 moge_status_t moge_combine(const moge_config_t *cfg, const void *y_perm, const int32_t *pair_row,
@@ -257,12 +259,18 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
     cudaError_t e = launch_permute(idx, cfg->T, K, cfg->N, counts, offsets, pair_row, row_token,
                                    at<int32_t>(ws, L.chunk_counts), at<uint32_t>(ws, L.status), st, cfg->M,
                                    a.group_load, a.score);
+    // Few tokens (weights-as-M tiles): the gate/up GEMM gathers the token rows itself (TMA gather4
+    // through row_token) and the gather stage is empty.  Many tokens: 32 gather4 copies per
+    // k-block would throttle the TMA unit, so rows are first copied to x_perm and loaded as tiles.
+    const bool gather_in_gemm = gathers_in_gemm(*cfg);
     mark_stage(MOGE_STAGE_GATHER, st);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !gather_in_gemm)
         e = launch_gather_rows(x, row_token, offsets, cfg->N, P, cfg->d, cfg->act_dtype, x_perm, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark_stage(MOGE_STAGE_GATE_UP, st);  // the FFN marks MOGE_STAGE_DOWN between its two GEMMs
-    if ((s = ffn_impl(cfg, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, st)) != MOGE_OK) return s;
+    s = gather_in_gemm ? ffn_impl(cfg, x, row_token, offsets, w_gate, w_up, w_down, y_perm, ws, st)
+                       : ffn_impl(cfg, x_perm, nullptr, offsets, w_gate, w_up, w_down, y_perm, ws, st);
+    if (s != MOGE_OK) return s;
     mark_stage(MOGE_STAGE_COMBINE, st);
     e = launch_combine(y_perm, pair_row, gate, cfg->T, K, cfg->d, cfg->act_dtype, y, st);
     mark_stage(MOGE_STAGE_IMBALANCE, st);  // empty: computed with the permutation

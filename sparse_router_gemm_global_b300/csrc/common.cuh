@@ -72,6 +72,10 @@ inline int router_kslices(int64_t T, int64_t d, int64_t N) {
     return s < 1 ? 1 : (int)s;
 }
 
+// bf16 layers with T <= 64 use weights-as-M tiles whose producer gathers token rows from x
+// (TMA gather4); every other layer reads a permuted copy x_perm.
+inline bool gathers_in_gemm(const moge_config_t &c) { return c.act_dtype == MOGE_BF16 && c.T <= 64; }
+
 inline WsLayout ws_layout(const moge_config_t &c) {
     const int64_t K = c.M * c.k_per_group;
     const int64_t P = c.T * K;
@@ -93,7 +97,8 @@ inline WsLayout ws_layout(const moge_config_t &c) {
         const int s = router_kslices(c.T, c.d, c.N);
         L.router_partials = take(s > 1 ? (size_t)cdiv(c.T, kRouterTileRows) * s * kRouterTileRows * c.N * 4 : 0);
     }
-    L.x_perm = take((size_t)P * c.d * es);
+    // layers whose gate/up GEMM gathers token rows itself store no permuted copy of x
+    L.x_perm = take(gathers_in_gemm(c) ? 0 : (size_t)P * c.d * es);
     L.h = take((size_t)P * c.I * es);
     L.y_perm = take((size_t)P * c.d * es);
     L.total = off;

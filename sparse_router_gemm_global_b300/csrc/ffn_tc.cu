@@ -72,6 +72,7 @@ struct Params {
     int out_dim;             // output features (I for gate/up, d for down)
     __nv_bfloat16 *out;      // [P, out_dim]
     uint32_t *status;        // workspace status word
+    const int32_t *row_token;  // [P] token of each permuted row (gathering launches only)
 };
 
 // prefix[e] = sum over e' < e of ceil(count_e' / tok_block); all 256 threads, N <= 1024.
@@ -135,7 +136,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-template <int MODE, int BNT>
+template <int MODE, int BNT, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
               const __grid_constant__ CUtensorMap map_b1, const Params p) {
@@ -187,43 +188,71 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     volatile int *abort_v = &abort_flag;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer (one thread)
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                int e, tb, fb;
-                tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
-                const int tok0 = p.offsets[e] + tb * C::tok_block;
-                const int f0 = fb * C::feat_block;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int s = it % C::stages;
-                    const uint32_t ph = (it / C::stages) & 1;
-                    if (!wait_bar(smem_u32(&empty_bar[s]), ph ^ 1, abort_v, p.status)) { ok = false; break; }
-                    const uint32_t fb_ = smem_u32(&full_bar[s]);
-                    const uint32_t sa = smem_base + s * C::stage_bytes;
-                    const uint32_t sb = sa + C::a_tiles * C::a_bytes;
-                    mbar_arrive_expect_tx(fb_, C::stage_bytes);
-                    const int k0 = kb * kBK;
-                    if constexpr (!C::swap) {
-                        tma_load_2d(sa, &map_a, fb_, k0, tok0);                          // token rows
-                        if constexpr (C::glu) {
-                            tma_load_3d(sb, &map_b0, fb_, k0, f0, e);                    // W_gate rows
-                            tma_load_3d(sb + 128 * 128, &map_b1, fb_, k0, f0, e);        // W_up rows
-                        } else {
-                            tma_load_3d(sb, &map_b0, fb_, k0, f0, e);                    // W_down rows
-                        }
+        // ------------------------------------------------ TMA producer
+        // Lane 0 owns the barriers and the weight loads.  With GATHER the token rows of the tile
+        // come straight from x (map_a has a one-row box): lane i gathers tile rows 4i..4i+3 with
+        // one tile::gather4 copy per k-block, through the row -> token map; otherwise lane 0 loads
+        // the rows of the already permuted matrix as one tile.
+        constexpr int tile_rows = C::swap ? (BNT > 0 ? BNT : 16) : kBM;
+        const bool gather_lane = GATHER && lane * 4 < tile_rows;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            int e, tb, fb;
+            tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
+            const int tok0 = p.offsets[e] + tb * C::tok_block;
+            const int f0 = fb * C::feat_block;
+            int r4[4] = {0, 0, 0, 0};
+            if (gather_lane) {
+                const int last = p.offsets[e + 1] - 1;  // rows past the expert repeat its last row
+#pragma unroll
+                for (int j = 0; j < 4; ++j) r4[j] = p.row_token[min(tok0 + lane * 4 + j, last)];
+            }
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % C::stages;
+                const uint32_t ph = (it / C::stages) & 1;
+                const uint32_t fb_ = smem_u32(&full_bar[s]);
+                int go = 1;
+                if (lane == 0) {
+                    go = wait_bar(smem_u32(&empty_bar[s]), ph ^ 1, abort_v, p.status);
+                    if (go) mbar_arrive_expect_tx(fb_, C::stage_bytes);
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) { ok = false; break; }
+                const uint32_t sa = smem_base + s * C::stage_bytes;
+                const uint32_t sb = sa + C::a_tiles * C::a_bytes;
+                const int k0 = kb * kBK;
+                if constexpr (!C::swap) {
+                    if constexpr (GATHER) {
+                        if (gather_lane) tma_gather4(sa + lane * 512, &map_a, fb_, k0, r4[0], r4[1], r4[2], r4[3]);
                     } else {
-                        tma_load_3d(sa, &map_b0, fb_, k0, f0, e);                        // W_gate / W_down
-                        if (C::glu) tma_load_3d(sa + C::a_bytes, &map_b1, fb_, k0, f0, e); // W_up
-                        tma_load_2d(sb, &map_a, fb_, k0, tok0);                          // token rows
+                        if (lane == 0) tma_load_2d(sa, &map_a, fb_, k0, tok0);               // token rows
+                    }
+                    if (lane == 0) {
+                        if constexpr (C::glu) {
+                            tma_load_3d(sb, &map_b0, fb_, k0, f0, e);                        // W_gate rows
+                            tma_load_3d(sb + 128 * 128, &map_b1, fb_, k0, f0, e);            // W_up rows
+                        } else {
+                            tma_load_3d(sb, &map_b0, fb_, k0, f0, e);                        // W_down rows
+                        }
+                    }
+                } else {
+                    if (lane == 0) {
+                        tma_load_3d(sa, &map_b0, fb_, k0, f0, e);                            // W_gate / W_down
+                        if (C::glu) tma_load_3d(sa + C::a_bytes, &map_b1, fb_, k0, f0, e);  // W_up
+                    }
+                    if constexpr (GATHER) {
+                        if (gather_lane) tma_gather4(sb + lane * 512, &map_a, fb_, k0, r4[0], r4[1], r4[2], r4[3]);
+                    } else {
+                        if (lane == 0) tma_load_2d(sb, &map_a, fb_, k0, tok0);               // token rows
                     }
                 }
             }
-            // drain: the last fill of every stage must have landed before the CTA may exit
+        }
+        // drain: the last fill of every stage must have landed before the CTA may exit
+        if (lane == 0)
             for (uint32_t j = (it > (uint32_t)C::stages ? it - C::stages : 0); j < it; ++j)
                 drain_wait(smem_u32(&full_bar[j % C::stages]), (j / C::stages) & 1, p.status);
-        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one thread)
@@ -425,11 +454,11 @@ int sm_count() {
     return n;
 }
 
-template <int MODE, int BNT>
+template <int MODE, int BNT, bool GATHER>
 cudaError_t launch_mode(const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1, const Params &p,
                         int64_t tile_bound, cudaStream_t s) {
     using C = Cfg<MODE, BNT>;
-    auto kern = ffn_tc_kernel<MODE, BNT>;
+    auto kern = ffn_tc_kernel<MODE, BNT, GATHER>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes);
     if (err != cudaSuccess) return err;
     const int grid = (int)std::min<int64_t>(tile_bound, (int64_t)sm_count());
@@ -439,22 +468,31 @@ cudaError_t launch_mode(const CUtensorMap &ma, const CUtensorMap &mb0, const CUt
     return cudaGetLastError();
 }
 
+// Token rows of the gate/up GEMM: gathered from x [T, d] through row_token (one-row box), or
+// read from the already permuted x_perm [P, d] (box of `rows` rows).
+bool make_act_map(CUtensorMap *m, const void *act, const int32_t *row_token, int64_t T, int64_t P, int64_t d,
+                  int rows) {
+    return row_token ? make_map_2d(m, act, T, d, 1) : make_map_2d(m, act, P, d, rows);
+}
+
 template <int BNT>
-cudaError_t launch_swap(const void *x_perm, const int32_t *offsets, int64_t N, int64_t P, int64_t d, int64_t I,
-                        const void *wg, const void *wu, const void *wd, void *h, void *y_perm, uint32_t *status,
-                        cudaStream_t s) {
+cudaError_t launch_swap(const void *act, const int32_t *row_token, const int32_t *offsets, int64_t N, int64_t P,
+                        int64_t T, int64_t d, int64_t I, const void *wg, const void *wu, const void *wd, void *h,
+                        void *y_perm, uint32_t *status, cudaStream_t s) {
     CUtensorMap mx, mh, mg, mu, mdn;
-    if (!make_map_2d(&mx, x_perm, P, d, BNT) || !make_map_2d(&mh, h, P, I, BNT) ||
+    if (!make_act_map(&mx, act, row_token, T, P, d, BNT) || !make_map_2d(&mh, h, P, I, BNT) ||
         !make_map_3d(&mg, wg, N, I, d, kBM) || !make_map_3d(&mu, wu, N, I, d, kBM) ||
         !make_map_3d(&mdn, wd, N, d, I, kBM))
         return cudaErrorInvalidValue;
     const int64_t tok_blocks = cdiv(P, BNT) + N;
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status};
-    cudaError_t err = launch_mode<SWAP_GLU, BNT>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s);
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token};
+    cudaError_t err = row_token
+        ? launch_mode<SWAP_GLU, BNT, true>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s)
+        : launch_mode<SWAP_GLU, BNT, false>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s);
     if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
-    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status};
-    return launch_mode<SWAP_PLAIN, BNT>(mh, mdn, mdn, p2, tok_blocks * cdiv(d, 128), s);
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr};
+    return launch_mode<SWAP_PLAIN, BNT, false>(mh, mdn, mdn, p2, tok_blocks * cdiv(d, 128), s);
 }
 
 }  // namespace tc
@@ -474,29 +512,34 @@ void *tensor_map_encoder() {
     return fn;
 }
 
-cudaError_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, int64_t N, int64_t P, int64_t T, int64_t d,
-                          int64_t I, const void *w_gate, const void *w_up, const void *w_down, void *h,
-                          void *y_perm, uint32_t *status, cudaStream_t s) {
+cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32_t *offsets, int64_t N, int64_t P,
+                          int64_t T, int64_t d, int64_t I, const void *w_gate, const void *w_up, const void *w_down,
+                          void *h, void *y_perm, uint32_t *status, cudaStream_t s) {
     using namespace tc;
     if (P == 0) return cudaSuccess;
     if (N > kMaxExperts) return cudaErrorInvalidValue;
     // A token selects an expert at most once, so no expert has more than T rows: with T <= 64
     // every expert fits one weights-as-M tile column.
-    if (T <= 16) return launch_swap<16>(x_perm, offsets, N, P, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
-    if (T <= 32) return launch_swap<32>(x_perm, offsets, N, P, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
-    if (T <= 64) return launch_swap<64>(x_perm, offsets, N, P, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
+    if (T <= 16)
+        return launch_swap<16>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
+    if (T <= 32)
+        return launch_swap<32>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
+    if (T <= 64)
+        return launch_swap<64>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
     CUtensorMap mx, mh, mg, mu, mdn;
-    if (!make_map_2d(&mx, x_perm, P, d, kBM) || !make_map_2d(&mh, h, P, I, kBM) ||
+    if (!make_act_map(&mx, act, row_token, T, P, d, kBM) || !make_map_2d(&mh, h, P, I, kBM) ||
         !make_map_3d(&mg, w_gate, N, I, d, 128) || !make_map_3d(&mu, w_up, N, I, d, 128) ||
         !make_map_3d(&mdn, w_down, N, d, I, 256))
         return cudaErrorInvalidValue;
     const int64_t row_blocks = cdiv(P, kBM) + N;
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status};
-    cudaError_t err = launch_mode<NORMAL_GLU, 0>(mx, mg, mu, p1, row_blocks * cdiv(I, 128), s);
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token};
+    cudaError_t err = row_token
+        ? launch_mode<NORMAL_GLU, 0, true>(mx, mg, mu, p1, row_blocks * cdiv(I, 128), s)
+        : launch_mode<NORMAL_GLU, 0, false>(mx, mg, mu, p1, row_blocks * cdiv(I, 128), s);
     if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
-    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status};
-    return launch_mode<NORMAL_PLAIN, 0>(mh, mdn, mdn, p2, row_blocks * cdiv(d, 256), s);
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr};
+    return launch_mode<NORMAL_PLAIN, 0, false>(mh, mdn, mdn, p2, row_blocks * cdiv(d, 256), s);
 }
 
 }  // namespace moge
