@@ -410,6 +410,208 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------------------------
+// Tokens-as-M tiles on CTA pairs (cluster of 2, tcgen05 cta_group::2).
+//
+// One MMA covers 256 token rows x 256 outputs: each CTA of the pair loads its 128 token rows
+// and half of the 256 weight rows (gate/up: the even CTA W_gate, the odd CTA W_up; down: 128
+// W_down rows each), so a k-block costs each SM 32 KB instead of 48 KB and the ring holds six
+// stages.  The even CTA's thread issues the MMAs; its full barrier counts the bytes of both
+// CTAs' copies (signalled across the pair), its commits arrive on both CTAs' empty and
+// accumulator-full barriers, and both CTAs' epilogue warps arrive on its accumulator-empty
+// barrier.  Each CTA's TMEM holds its own 128 rows x 256 fp32 columns (double buffered).
+// ---------------------------------------------------------------------------------------------
+constexpr int kPairRows = 256;                   // token rows per pair tile
+constexpr int kPairStageBytes = 2 * kBM * 128;   // per CTA: 128 token rows + 128 weight rows
+constexpr int kPairStages = 6;
+constexpr size_t kPairSmem = (size_t)kPairStages * kPairStageBytes + 1024;
+constexpr uint32_t kPairIdesc = idesc_bf16_f32(256, 256);
+constexpr int kPairTmemCols = 512;               // two 256-column accumulators
+
+template <bool GLU>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                   const __grid_constant__ CUtensorMap map_b1, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int32_t prefix[kMaxExperts + 1];
+    __shared__ int32_t warp_sums[8];
+    __shared__ __align__(8) uint64_t full_bar[kPairStages], empty_bar[kPairStages];
+    __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t smem_base = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull_bar[b]), 1);
+            mbar_init(smem_u32(&tempty_bar[b]), 8);  // 4 epilogue warps of each CTA
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b0);
+        if (GLU) tma_prefetch_desc(&map_b1);
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(smem_u32(&tmem_base_slot), kPairTmemCols);
+        tmem_relinquish_pair();
+    }
+    build_prefix(p.offsets, p.N, kPairRows, prefix, warp_sums);  // contains __syncthreads
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers are initialised and their TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_slot;
+
+    constexpr int feat_block = GLU ? 128 : 256;
+    const int nfb = (p.out_dim + feat_block - 1) / feat_block;
+    const int total_tiles = prefix[p.N] * nfb;
+    const int kblocks = (p.kdim + kBK - 1) / kBK;
+    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    volatile int *abort_v = &abort_flag;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (one thread per CTA)
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = cid; tile < total_tiles && ok; tile += ncl) {
+                int e, pb, fb;
+                tile_coords(tile, nfb, prefix, p.N, e, pb, fb);
+                const int rows0 = p.offsets[e] + pb * kPairRows + (int)rank * kBM;
+                const int f0 = fb * feat_block + (GLU ? 0 : (int)rank * kBM);
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % kPairStages;
+                    const uint32_t ph = (it / kPairStages) & 1;
+                    if (!wait_bar(smem_u32(&empty_bar[s]), ph ^ 1, abort_v, p.status)) { ok = false; break; }
+                    const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * kPairStageBytes);
+                    const uint32_t sa = smem_base + s * kPairStageBytes;
+                    const uint32_t sb = sa + kBM * 128;
+                    const int k0 = kb * kBK;
+                    tma_load_2d_pair(sa, &map_a, full_leader, k0, rows0);                // 128 token rows
+                    if (GLU && !leader) tma_load_3d_pair(sb, &map_b1, full_leader, k0, f0, e);  // W_up
+                    else tma_load_3d_pair(sb, &map_b0, full_leader, k0, f0, e);          // W_gate / W_down
+                }
+            }
+            // drain (even CTA): its full barriers also count the odd CTA's copies
+            if (leader)
+                for (uint32_t j = (it > (uint32_t)kPairStages ? it - kPairStages : 0); j < it; ++j)
+                    drain_wait(smem_u32(&full_bar[j % kPairStages]), (j / kPairStages) & 1, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (one thread, even CTA)
+        if (lane == 0 && leader) {
+            uint32_t it = 0, local = 0;
+            bool ok = true;
+            for (int tile = cid; tile < total_tiles && ok; tile += ncl, ++local) {
+                const int acc = local & 1;
+                const uint32_t use = local >> 1;
+                if (!wait_bar(smem_u32(&tempty_bar[acc]), (use & 1) ^ 1, abort_v, p.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * 256;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % kPairStages;
+                    const uint32_t ph = (it / kPairStages) & 1;
+                    if (!wait_bar(smem_u32(&full_bar[s]), ph, abort_v, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_base + s * kPairStageBytes;
+                    const uint32_t sb = sa + kBM * 128;
+#pragma unroll
+                    for (int j = 0; j < kBK / 16; ++j)
+                        mma_bf16_pair(d_tmem, smem_desc_sw128(sa + j * 32), smem_desc_sw128(sb + j * 32), kPairIdesc,
+                                      (kb > 0 || j > 0) ? 1u : 0u);
+                    mma_commit_pair_mc(smem_u32(&empty_bar[s]), 0x3);  // frees the stage in both CTAs
+                }
+                if (!ok) break;
+                mma_commit_pair_mc(smem_u32(&tfull_bar[acc]), 0x3);    // accumulators ready in both CTAs
+            }
+            mma_commit_pair(smem_u32(&drain_bar));
+            drain_wait(smem_u32(&drain_bar), 0, p.status);
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+        // ------------------------------------------------ epilogue (warps 4..7 of each CTA)
+        const int q = warp & 3;
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        uint32_t local = 0;
+        for (int tile = cid; tile < total_tiles; tile += ncl, ++local) {
+            const int acc = local & 1;
+            const uint32_t use = local >> 1;
+            bool ok = wait_bar(smem_u32(&tfull_bar[acc]), use & 1, abort_v, p.status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            int e, pb, fb;
+            tile_coords(tile, nfb, prefix, p.N, e, pb, fb);
+            const int cnt = p.offsets[e + 1] - p.offsets[e];
+            const int r = (int)rank * kBM + q * 32 + lane;       // row inside the 256-row pair tile
+            const bool row_ok = r < cnt - pb * kPairRows;
+            __nv_bfloat16 *orow = p.out + (int64_t)(p.offsets[e] + pb * kPairRows + r) * p.out_dim;
+            const int f0 = fb * feat_block;
+            const uint32_t t_acc = tmem_base + acc * 256 + lane_addr;
+            constexpr int chunks = GLU ? 4 : 8;
+#pragma unroll 1
+            for (int c = 0; c < chunks; ++c) {
+                uint32_t va[32];
+                float o[32];
+                tmem_ld_x32(t_acc + c * 32, va);
+                if constexpr (GLU) {
+                    uint32_t vu[32];
+                    tmem_ld_x32(t_acc + 128 + c * 32, vu);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = swiglu_fast(__uint_as_float(va[j]), __uint_as_float(vu[j]));
+                } else {
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(va[j]);
+                }
+                const int col0 = f0 + c * 32;
+                if (row_ok) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int col = col0 + v * 8;
+                        if (col < p.out_dim) {
+                            uint4 pk;
+                            pk.x = pack_bf16x2(o[v * 8 + 0], o[v * 8 + 1]);
+                            pk.y = pack_bf16x2(o[v * 8 + 2], o[v * 8 + 3]);
+                            pk.z = pack_bf16x2(o[v * 8 + 4], o[v * 8 + 5]);
+                            pk.w = pack_bf16x2(o[v * 8 + 6], o[v * 8 + 7]);
+                            *reinterpret_cast<uint4 *>(orow + col) = pk;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(smem_u32(&tempty_bar[acc]));
+                else mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the odd CTA's shared memory and TMEM stay live until the even CTA's MMAs end
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc_pair(tmem_base, kPairTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------------
 // Host side: tensor maps and launches
 // ---------------------------------------------------------------------------------------------
 
@@ -464,6 +666,19 @@ cudaError_t launch_mode(const CUtensorMap &ma, const CUtensorMap &mb0, const CUt
     const int grid = (int)std::min<int64_t>(tile_bound, (int64_t)sm_count());
     if (grid <= 0) return cudaSuccess;
     kern<<<grid, kThreads, C::smem_bytes, s>>>(ma, mb0, mb1, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <bool GLU>
+cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1, const Params &p,
+                        int64_t pair_tile_bound, cudaStream_t s) {
+    auto kern = ffn_tc_pair_kernel<GLU>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem);
+    if (err != cudaSuccess) return err;
+    const int grid = (int)std::min<int64_t>(2 * pair_tile_bound, (int64_t)(sm_count() & ~1));  // whole pairs
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, kThreads, kPairSmem, s>>>(ma, mb0, mb1, p);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -526,20 +741,20 @@ cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32
         return launch_swap<32>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
     if (T <= 64)
         return launch_swap<64>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
+    // many tokens: tokens-as-M tiles of 256 rows on CTA pairs, rows read from x_perm
+    if (row_token) return cudaErrorInvalidValue;
     CUtensorMap mx, mh, mg, mu, mdn;
-    if (!make_act_map(&mx, act, row_token, T, P, d, kBM) || !make_map_2d(&mh, h, P, I, kBM) ||
-        !make_map_3d(&mg, w_gate, N, I, d, 128) || !make_map_3d(&mu, w_up, N, I, d, 128) ||
-        !make_map_3d(&mdn, w_down, N, d, I, 256))
+    if (!make_map_2d(&mx, act, P, d, kBM) || !make_map_2d(&mh, h, P, I, kBM) ||
+        !make_map_3d(&mg, w_gate, N, I, d, kBM) || !make_map_3d(&mu, w_up, N, I, d, kBM) ||
+        !make_map_3d(&mdn, w_down, N, d, I, kBM))
         return cudaErrorInvalidValue;
-    const int64_t row_blocks = cdiv(P, kBM) + N;
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token};
-    cudaError_t err = row_token
-        ? launch_mode<NORMAL_GLU, 0, true>(mx, mg, mu, p1, row_blocks * cdiv(I, 128), s)
-        : launch_mode<NORMAL_GLU, 0, false>(mx, mg, mu, p1, row_blocks * cdiv(I, 128), s);
+    const int64_t pair_blocks = cdiv(P, kPairRows) + N;  // bound of sum_e ceil(count_e / 256)
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, nullptr};
+    cudaError_t err = launch_pair<true>(mx, mg, mu, p1, pair_blocks * cdiv(I, 128), s);
     if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
     Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr};
-    return launch_mode<NORMAL_PLAIN, 0, false>(mh, mdn, mdn, p2, row_blocks * cdiv(d, 256), s);
+    return launch_pair<false>(mh, mdn, mdn, p2, pair_blocks * cdiv(d, 256), s);
 }
 
 }  // namespace moge
