@@ -171,15 +171,25 @@ class Layer:
                                      d["w_up"], d["w_down"], self.y if y is None else y, self.ws, aux=self.aux)
 
 
-def timed_steps(layer, steps, warmup, dist, stage_events=True):
-    """K steps bracketed by barrier + synchronize; returns (ms/step max over ranks, stage ms means)."""
+def timed_steps(layer, steps, warmup, dist):
+    """K steps bracketed by barrier + synchronize.  Inside the timed region the library records
+    only the two events around the grouped gate/up GEMM (the roofline kernel), on its own
+    stream, so that the step time carries no instrumentation of the other stages.
+    Returns (ms/step max over ranks, gate/up ms per launch, kernel launches in the region)."""
     import torch
     moge = layer.moge
     for _ in range(warmup):
         layer.step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moge.MOGE_NUM_STAGES + 1)]
-           for _ in range(steps)] if stage_events else None
+    gu, dn = moge.STAGE_NAMES.index("gate_up"), moge.STAGE_NAMES.index("down")
+    evs = []
+    for _ in range(steps):
+        row = [None] * (moge.MOGE_NUM_STAGES + 1)
+        row[gu], row[gu + 1] = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for e in (row[gu], row[gu + 1]):
+            e.record()  # torch creates the CUDA event on first record: do that outside the timed region
+        evs.append(row)
+    assert gu + 1 == dn
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         torch.distributed.barrier()
@@ -187,13 +197,11 @@ def timed_steps(layer, steps, warmup, dist, stage_events=True):
     n0 = moge.moge_kernel_launch_count()
     start.record()
     for i in range(steps):
-        if evs is not None:
-            moge.moge_set_stage_events(evs[i])
+        moge.moge_set_stage_events(evs[i])
         layer.step()
     end.record()
     torch.cuda.synchronize()
-    if evs is not None:
-        moge.moge_set_stage_events(None)
+    moge.moge_set_stage_events(None)
     launches = moge.moge_kernel_launch_count() - n0
     if dist:
         torch.distributed.barrier()
@@ -202,14 +210,26 @@ def timed_steps(layer, steps, warmup, dist, stage_events=True):
         t = torch.tensor([ms], device=layer.dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    stages = None
-    if evs is not None:
-        stages = {}
-        for s, name in enumerate(moge.STAGE_NAMES):
-            stages[name] = statistics.fmean(e[s].elapsed_time(e[s + 1]) for e in evs)
+    gate_up_ms = statistics.fmean(e[gu].elapsed_time(e[gu + 1]) for e in evs)
     if moge.moge_query_device_status(layer.ws) != 0:
         raise RuntimeError("device status reports a timed-out wait")
-    return ms, stages, launches
+    return ms, gate_up_ms, launches
+
+
+def stage_breakdown(layer, steps):
+    """Device time of every stage (events at every stage boundary; outside the timed region,
+    since each recorded event adds a few microseconds to the step)."""
+    import torch
+    moge = layer.moge
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moge.MOGE_NUM_STAGES + 1)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        moge.moge_set_stage_events(evs[i])
+        layer.step()
+    torch.cuda.synchronize()
+    moge.moge_set_stage_events(None)
+    return {name: round(statistics.fmean(e[s].elapsed_time(e[s + 1]) for e in evs), 5)
+            for s, name in enumerate(moge.STAGE_NAMES)}
 
 
 def e2e_steps(layer, steps, dist):
@@ -356,8 +376,9 @@ def run_ours(args):
         os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
     gpu_index = int(phys) if phys.isdigit() else local
     with ClockSampler(gpu_index) as clk:
-        ms, stages, launches = timed_steps(prefill, args.steps, args.warmup, dist)
+        ms, gate_up_ms, launches = timed_steps(prefill, args.steps, args.warmup, dist)
     clocks = clk.summary()
+    stages = stage_breakdown(prefill, min(args.steps, 50))
     counts = prefill.aux["counts"].cpu().numpy()
     score = float(prefill.aux["score"][0].item())
 
@@ -365,13 +386,14 @@ def run_ours(args):
     decode = None
     if args.decode_steps > 0:
         dec = Layer(wd, d_inp, device)
-        dms, dstages, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist)
+        dms, dgate_up_ms, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist)
+        dstages = stage_breakdown(dec, min(args.decode_steps, 100))
         dcounts = dec.aux["counts"].cpu().numpy()
         decode = {"workload": wd.name, "value": round(wd.T * ws_n / (dms / 1e3), 1), "unit": "tokens/s",
                   "ms_per_step": round(dms, 4), "steps": args.decode_steps,
-                  "roofline": gate_up_roofline(wd, dcounts, dstages["gate_up"], pk, peak_kind),
+                  "roofline": gate_up_roofline(wd, dcounts, dgate_up_ms, pk, peak_kind),
                   "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
-                  "stage_ms": {k: round(v, 5) for k, v in dstages.items()}, "gpu_launches": int(dlaunches)}
+                  "stage_ms": dstages, "gpu_launches": int(dlaunches)}
 
     # end to end through the public call with host buffers
     e2e = None
@@ -399,9 +421,9 @@ def run_ours(args):
         "config": {"workload": wp.name, "T": wp.T, "d": wp.d, "N": wp.N, "M": wp.M, "k_per_group": wp.kpg,
                    "K": wp.K, "I": wp.I, "seed": DEFAULT_SEED, "parallelism": f"replicas x{ws_n}",
                    "l2": "inputs larger than L2 (2.2 GB of expert weights, 1 GB permuted activations)"},
-        "roofline": gate_up_roofline(wp, counts, stages["gate_up"], pk, peak_kind),
+        "roofline": gate_up_roofline(wp, counts, gate_up_ms, pk, peak_kind),
         "layer_roofline": layer_roofline(wp, counts, ms, pk),
-        "stage_ms": {k: round(v, 5) for k, v in stages.items()},
+        "stage_ms": stages,
         "imbalance_score": score,
         "clocks": clocks,
         "e2e": e2e,

@@ -223,8 +223,10 @@ typedef enum {
  * (cudaEvent_t handles owned by the caller) on its stream right before stage i
  * and events[MOGE_NUM_STAGES] after the last stage, so that
  * cudaEventElapsedTime(events[i], events[i+1]) is the device time of stage i.
- * n must be MOGE_NUM_STAGES + 1; events == NULL turns recording off.  The
- * array is read at each call, so it must stay valid while recording is on. */
+ * n must be MOGE_NUM_STAGES + 1; a NULL entry skips that boundary (each
+ * recorded event costs a few microseconds of device time, so time one stage
+ * by setting only its two boundaries); events == NULL turns recording off.
+ * The array is read at each call, so it must stay valid while recording is on. */
 moge_status_t moge_set_stage_events(void *const *events, int n);
 
 /* Number of kernels this library has launched since it was loaded (all host

@@ -183,8 +183,9 @@ STAGE_NAMES = ("route", "permute", "gather", "gate_up", "down", "combine", "imba
 
 
 def moge_set_stage_events(events) -> None:
-    """events: None, or a list of MOGE_NUM_STAGES+1 torch.cuda.Event (created with timing on).
-    The ctypes array is kept alive by the binding while recording is on."""
+    """events: None, or a list of MOGE_NUM_STAGES+1 entries, each a torch.cuda.Event (created with
+    timing on) or None (that boundary is not recorded).  The ctypes array is kept alive by the
+    binding while recording is on."""
     global _stage_array
     lib = load()
     if events is None:
@@ -193,6 +194,9 @@ def moge_set_stage_events(events) -> None:
         return
     handles = []
     for ev in events:
+        if ev is None:
+            handles.append(None)
+            continue
         if not ev.cuda_event:
             ev.record()  # torch creates the underlying cudaEvent_t lazily, on first record
         handles.append(ev.cuda_event)

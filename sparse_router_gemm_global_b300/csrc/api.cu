@@ -18,7 +18,7 @@ thread_local void *const *t_stage_events = nullptr;
 namespace moge {
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 void mark_stage(int stage, cudaStream_t s) {
-    if (t_stage_events && stage >= 0 && stage <= MOGE_NUM_STAGES)
+    if (t_stage_events && stage >= 0 && stage <= MOGE_NUM_STAGES && t_stage_events[stage])
         cudaEventRecord((cudaEvent_t)t_stage_events[stage], s);
 }
 }  // namespace moge
@@ -75,6 +75,12 @@ moge_status_t route_impl(const moge_config_t *c, moge_route_mode_t mode, const v
     const WsLayout L = ws_layout(*c);
     const float *scores = logits;
     const bool global = mode == MOGE_ROUTE_GLOBAL_TOPK;
+    const int64_t K = c->M * c->k_per_group;
+    if (x && route_small_fits(c->T, c->N, K, c->M, false))  // few tokens: CUDA cores, one launch
+        return cuda_status(launch_route_small(x, w_router, bias, c->T, c->d, c->N, c->M, c->k_per_group, global,
+                                              c->act_dtype, at<float>(ws, L.logits), logits, idx, gate,
+                                              at<uint32_t>(ws, kTicketOffset), at<uint32_t>(ws, L.status),
+                                              nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, st));
     if (x && c->act_dtype == MOGE_BF16 && c->N <= 256)  // scores, softmax and selection in one launch
         return cuda_status(launch_router_tc(x, w_router, bias, c->T, c->d, c->N, c->M, c->k_per_group, global,
                                             logits, idx, gate, at<float>(ws, L.router_partials),
@@ -253,12 +259,23 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
     void *y_perm = at<void>(ws, L.y_perm);
 
     mark_stage(MOGE_STAGE_ROUTE, st);
-    if ((s = route_impl(cfg, MOGE_ROUTE_GROUPED, x, w_router, bias, a.logits, idx, gate, ws, st)) != MOGE_OK)
-        return s;
-    mark_stage(MOGE_STAGE_PERMUTE, st);  // the permutation also writes the imbalance outputs
-    cudaError_t e = launch_permute(idx, cfg->T, K, cfg->N, counts, offsets, pair_row, row_token,
-                                   at<int32_t>(ws, L.chunk_counts), at<uint32_t>(ws, L.status), st, cfg->M,
-                                   a.group_load, a.score);
+    cudaError_t e = cudaSuccess;
+    if (route_small_fits(cfg->T, cfg->N, K, cfg->M, true)) {
+        // few tokens: routing and permutation in one launch; the permutation stage is empty
+        e = launch_route_small(x, w_router, bias, cfg->T, cfg->d, cfg->N, cfg->M, cfg->k_per_group, false,
+                               cfg->act_dtype, at<float>(ws, L.logits), a.logits, idx, gate,
+                               at<uint32_t>(ws, kTicketOffset), at<uint32_t>(ws, L.status), counts, offsets,
+                               pair_row, row_token, a.group_load, a.score, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        mark_stage(MOGE_STAGE_PERMUTE, st);
+    } else {
+        if ((s = route_impl(cfg, MOGE_ROUTE_GROUPED, x, w_router, bias, a.logits, idx, gate, ws, st)) != MOGE_OK)
+            return s;
+        mark_stage(MOGE_STAGE_PERMUTE, st);  // the permutation also writes the imbalance outputs
+        e = launch_permute(idx, cfg->T, K, cfg->N, counts, offsets, pair_row, row_token,
+                           at<int32_t>(ws, L.chunk_counts), at<uint32_t>(ws, L.status), st, cfg->M, a.group_load,
+                           a.score);
+    }
     // Few tokens (weights-as-M tiles): the gate/up GEMM gathers the token rows itself (TMA gather4
     // through row_token) and the gather stage is empty.  Many tokens: 32 gather4 copies per
     // k-block would throttle the TMA unit, so rows are first copied to x_perm and loaded as tiles.
@@ -280,9 +297,6 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
 
 moge_status_t moge_set_stage_events(void *const *events, int n) {
     if (events && n != MOGE_NUM_STAGES + 1) return MOGE_ERR_INVALID_ARGUMENT;
-    if (events)
-        for (int i = 0; i < n; ++i)
-            if (!events[i]) return MOGE_ERR_INVALID_ARGUMENT;
     t_stage_events = events;
     return MOGE_OK;
 }

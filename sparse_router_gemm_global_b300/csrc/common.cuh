@@ -72,6 +72,12 @@ inline int router_kslices(int64_t T, int64_t d, int64_t N) {
     return s < 1 ? 1 : (int)s;
 }
 
+// Batches of at most kSmallRouteMaxT tokens are routed (and, inside the layer, permuted) by one
+// CUDA-core launch (route_small.cu) when its shared-memory staging fits kSmallRouteMaxSmem.
+constexpr int kSmallRouteMaxT = 64;
+constexpr size_t kSmallRouteMaxSmem = 160 * 1024;
+static_assert(kSmallRouteMaxT <= kPermuteChunk, "the small router permutes its tokens in one block");
+
 // bf16 layers with T <= 64 use weights-as-M tiles whose producer gathers token rows from x
 // (TMA gather4); every other layer reads a permuted copy x_perm.
 inline bool gathers_in_gemm(const moge_config_t &c) { return c.act_dtype == MOGE_BF16 && c.T <= 64; }
@@ -117,6 +123,14 @@ void *tensor_map_encoder();
 cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, int64_t T, int64_t d, int64_t N,
                              int64_t M, int64_t kpg, bool global, float *logits_out, int32_t *idx, float *gate,
                              float *partials, uint32_t *tickets, uint32_t *status, cudaStream_t s);
+// Small-batch router (any dtype): scores, softmax, selection and, when counts != nullptr, the
+// permutation of all T tokens (+ group loads and imbalance score) in one launch.
+bool route_small_fits(int64_t T, int64_t N, int64_t K, int64_t M, bool permute);
+cudaError_t launch_route_small(const void *x, const void *w_r, const float *bias, int64_t T, int64_t d, int64_t N,
+                               int64_t M, int64_t kpg, bool global, int dtype, float *scores, float *logits_out,
+                               int32_t *idx, float *gate, uint32_t *ticket, uint32_t *status, int32_t *counts,
+                               int32_t *offsets, int32_t *pair_row, int32_t *row_token, int32_t *group_load,
+                               float *score, cudaStream_t s);
 cudaError_t launch_router_logits_simt(const void *x, const void *w_r, const float *bias, int64_t T,
                                       int64_t d, int64_t N, int dtype, float *logits, cudaStream_t s);
 cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, int32_t *counts,

@@ -1,79 +1,24 @@
 // Permutation of (token, slot) pairs into expert-contiguous rows:
 // histogram -> prefix sum -> deterministic scatter, then the row gather.
-//
-// Row of pair (t,k) with expert e:  offsets[e] + #{t' < t routed to e}.
-// Tokens are cut into chunks of kPermuteChunk (one block each, one token per
-// thread).  Inside a chunk, warp w publishes, for every expert, the bitmask of
-// its lanes routed there (shared atomicOr: order-free, so deterministic); the
-// rank of a lane among earlier lanes is popc(mask & lanemask_lt), the rank of a
-// warp's first lane is the sum of popc over earlier warps, and the chunk's base
-// is the sum over earlier chunks.  A token selects each expert at most once, so
-// "earlier pair with the same expert" equals "earlier token".
+// Tokens are cut into chunks of kPermuteChunk (one block each, one token per thread); the
+// block-level steps are in permute_block.cuh.
 #include <algorithm>
 
 #include "common.cuh"
+#include "permute_block.cuh"
 
 namespace moge {
-
-constexpr int kChunk = kPermuteChunk;
-constexpr int kWarps = kChunk / 32;
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    uint32_t m;
-    asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
-
-// Fill masks[w*N + e] for this block's chunk.  Returns nothing; caller syncs.
-__device__ __forceinline__ void build_masks(const int32_t *__restrict__ idx, int64_t T, int K, int N,
-                                            uint32_t *masks, uint32_t *status) {
-    for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) masks[i] = 0u;
-    __syncthreads();
-    const int64_t t = (int64_t)blockIdx.x * kChunk + threadIdx.x;
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (t < T) {
-        for (int k = 0; k < K; ++k) {
-            const int e = idx[t * K + k];
-            if (e >= 0 && e < N) atomicOr(&masks[w * N + e], 1u << lane);
-            else raise_status(status, kStatusBadIndex);
-        }
-    }
-}
 
 // Per-chunk expert counts: chunk_counts[chunk][e].
 __global__ void permute_count_kernel(const int32_t *__restrict__ idx, int64_t T, int K, int N,
                                      int32_t *__restrict__ chunk_counts, uint32_t *status) {
     extern __shared__ uint32_t masks[];  // [kWarps][N]
-    build_masks(idx, T, K, N, masks, status);
+    build_masks(idx, (int64_t)blockIdx.x * kChunk, T, K, N, masks, status);
     __syncthreads();
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
         int c = 0;
         for (int w = 0; w < kWarps; ++w) c += __popc(masks[w * N + e]);
         chunk_counts[(int64_t)blockIdx.x * N + e] = c;
-    }
-}
-
-// Optional imbalance score from per-expert counts in shared memory (the whole block calls it):
-// group_load[g] = sum of the counts of group g's experts, score = (max - min) / T (fp32).
-// `loads` is shared scratch of M ints.
-__device__ __forceinline__ void block_imbalance(const int32_t *cnt, int N, int M, int64_t T, int32_t *loads,
-                                                int32_t *__restrict__ group_load, float *__restrict__ score) {
-    if (!group_load && !score) return;
-    const int G = N / M;
-    for (int g = threadIdx.x; g < M; g += blockDim.x) {
-        int s = 0;
-        for (int e = g * G; e < (g + 1) * G; ++e) s += cnt[e];
-        loads[g] = s;
-        if (group_load) group_load[g] = s;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && score) {
-        int mx = loads[0], mn = loads[0];
-        for (int g = 1; g < M; ++g) {
-            mx = max(mx, loads[g]);
-            mn = min(mn, loads[g]);
-        }
-        *score = T > 0 ? (float)(mx - mn) / (float)T : 0.f;
     }
 }
 
@@ -104,33 +49,6 @@ __global__ void permute_scan_kernel(int32_t *__restrict__ chunk_counts, int chun
     block_imbalance(tot, N, M, T, tot + N, group_load, score);
 }
 
-// Rows of the chunk's pairs.  base[e] = offsets[e] + bases of earlier chunks.
-__device__ __forceinline__ void scatter_rows(const int32_t *__restrict__ idx, int64_t T, int K, int N,
-                                             const uint32_t *masks, int32_t *warp_base,
-                                             const int32_t *base, int32_t *__restrict__ pair_row,
-                                             int32_t *__restrict__ row_token) {
-    for (int e = threadIdx.x; e < N; e += blockDim.x) {
-        int run = base[e];
-        for (int w = 0; w < kWarps; ++w) {
-            warp_base[w * N + e] = run;
-            run += __popc(masks[w * N + e]);
-        }
-    }
-    __syncthreads();
-    const int64_t t = (int64_t)blockIdx.x * kChunk + threadIdx.x;
-    const int w = threadIdx.x >> 5;
-    const uint32_t lt = lanemask_lt();
-    if (t < T) {
-        for (int k = 0; k < K; ++k) {
-            const int e = idx[t * K + k];
-            int row = -1;
-            if (e >= 0 && e < N) row = warp_base[w * N + e] + __popc(masks[w * N + e] & lt);
-            if (pair_row) pair_row[t * K + k] = row;
-            if (row_token && row >= 0) row_token[row] = (int32_t)t;
-        }
-    }
-}
-
 __global__ void permute_scatter_kernel(const int32_t *__restrict__ idx, int64_t T, int K, int N,
                                        const int32_t *__restrict__ chunk_base,
                                        const int32_t *__restrict__ offsets, int32_t *__restrict__ pair_row,
@@ -139,11 +57,11 @@ __global__ void permute_scatter_kernel(const int32_t *__restrict__ idx, int64_t 
     uint32_t *masks = sm;                              // [kWarps][N]
     int32_t *warp_base = (int32_t *)(sm + kWarps * N);  // [kWarps][N]
     int32_t *base = warp_base + kWarps * N;             // [N]
-    build_masks(idx, T, K, N, masks, nullptr);
+    build_masks(idx, (int64_t)blockIdx.x * kChunk, T, K, N, masks, nullptr);
     for (int e = threadIdx.x; e < N; e += blockDim.x)
         base[e] = offsets[e] + chunk_base[(int64_t)blockIdx.x * N + e];
     __syncthreads();
-    scatter_rows(idx, T, K, N, masks, warp_base, base, pair_row, row_token);
+    scatter_rows(idx, (int64_t)blockIdx.x * kChunk, T, K, N, masks, warp_base, base, pair_row, row_token);
 }
 
 // T <= kChunk: count, scan and scatter in one block (+ imbalance).
@@ -153,33 +71,7 @@ __global__ void permute_single_kernel(const int32_t *__restrict__ idx, int64_t T
                                       uint32_t *status, int M, int32_t *__restrict__ group_load,
                                       float *__restrict__ score) {
     extern __shared__ uint32_t sm[];
-    uint32_t *masks = sm;
-    int32_t *warp_base = (int32_t *)(sm + kWarps * N);
-    int32_t *base = warp_base + kWarps * N;
-    int32_t *loads = base + N;
-    build_masks(idx, T, K, N, masks, status);
-    __syncthreads();
-    for (int e = threadIdx.x; e < N; e += blockDim.x) {
-        int c = 0;
-        for (int w = 0; w < kWarps; ++w) c += __popc(masks[w * N + e]);
-        base[e] = c;
-    }
-    __syncthreads();
-    block_imbalance(base, N, M, T, loads, group_load, score);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int e = 0; e < N; ++e) {
-            const int c = base[e];
-            counts[e] = c;
-            offsets[e] = run;
-            base[e] = run;
-            run += c;
-        }
-        offsets[N] = run;
-    }
-    __syncthreads();
-    scatter_rows(idx, T, K, N, masks, warp_base, base, pair_row, row_token);
+    permute_one_block(idx, T, K, N, counts, offsets, pair_row, row_token, status, M, group_load, score, sm);
 }
 
 __global__ void zero_counts_kernel(int N, int32_t *counts, int32_t *offsets, int M, int32_t *group_load,
@@ -201,7 +93,7 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
         count_launches(1);
         return cudaGetLastError();
     }
-    const size_t smem_scatter = (size_t)(2 * kWarps * N + N + M) * 4;
+    const size_t smem_scatter = (size_t)permute_block_smem_words((int)N, (int)M) * 4;
     cudaError_t err;
     if (T <= kChunk) {
         err = cudaFuncSetAttribute(permute_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
