@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import signal
 import statistics
 import subprocess
 import sys
@@ -76,9 +77,11 @@ def recorded_traffic(key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+    """nvidia-smi clocks/throttle sampling while the timed region runs.  Every sample carries
+    nvidia-smi's own timestamp, so only samples taken inside the marked region are summarised
+    (the tool's start-up time and output buffering do not matter)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -86,6 +89,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = os.path.join("/tmp", f"moge_clocks_{os.getpid()}.csv")
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         try:
@@ -93,14 +97,23 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            time.sleep(1.0)  # let the tool start before the region begins
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
+    def mark_start(self):
+        import datetime
+        self.t_start = datetime.datetime.now()
+
+    def mark_end(self):
+        import datetime
+        self.t_end = datetime.datetime.now()
+
     def __exit__(self, *exc):
         if self.proc is not None:
-            self.proc.terminate()
+            time.sleep(0.3)
+            self.proc.send_signal(signal.SIGINT)  # lets the tool flush its output
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
@@ -108,29 +121,35 @@ class ClockSampler:
             self.f.close()
 
     def summary(self):
+        import datetime
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                    power.append(float(parts[3]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
         os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        lo = self.t_start - datetime.timedelta(seconds=0.05) if self.t_start else None
+        hi = self.t_end + datetime.timedelta(seconds=0.15) if self.t_end else None
+        inside = [r for r in rows if lo is None or (lo <= r[0] <= hi)]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "samples_total": len(rows),
+                    "reasons": ["no sample inside the timed region"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[4]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "power_w_max": max(r[3] for r in inside), "samples": len(inside), "reasons": sorted(reasons)}
 
 
 # --------------------------------------------------------------------------------------------
@@ -171,7 +190,7 @@ class Layer:
                                      d["w_up"], d["w_down"], self.y if y is None else y, self.ws, aux=self.aux)
 
 
-def timed_steps(layer, steps, warmup, dist):
+def timed_steps(layer, steps, warmup, dist, clock=None):
     """K steps bracketed by barrier + synchronize.  Inside the timed region the library records
     only the two events around the grouped gate/up GEMM (the roofline kernel), on its own
     stream, so that the step time carries no instrumentation of the other stages.
@@ -195,12 +214,16 @@ def timed_steps(layer, steps, warmup, dist):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     n0 = moge.moge_kernel_launch_count()
+    if clock:
+        clock.mark_start()
     start.record()
     for i in range(steps):
         moge.moge_set_stage_events(evs[i])
         layer.step()
     end.record()
     torch.cuda.synchronize()
+    if clock:
+        clock.mark_end()
     moge.moge_set_stage_events(None)
     launches = moge.moge_kernel_launch_count() - n0
     if dist:
@@ -376,7 +399,7 @@ def run_ours(args):
         os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
     gpu_index = int(phys) if phys.isdigit() else local
     with ClockSampler(gpu_index) as clk:
-        ms, gate_up_ms, launches = timed_steps(prefill, args.steps, args.warmup, dist)
+        ms, gate_up_ms, launches = timed_steps(prefill, args.steps, args.warmup, dist, clock=clk)
     clocks = clk.summary()
     stages = stage_breakdown(prefill, min(args.steps, 50))
     counts = prefill.aux["counts"].cpu().numpy()
@@ -523,7 +546,7 @@ def record_traffic(csv_path: str, command: str) -> None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--decode-steps", type=int, default=300)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")

@@ -205,6 +205,27 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
                                  const void *w_down, void *y, const moge_aux_t *aux, void *ws,
                                  size_t ws_bytes, moge_stream_t stream);
 
+/* Monte-Carlo study of the imbalance score (Pangu Pro MoE explainer, section 1:
+ * a Monte-Carlo simulation finds the imbalance score of conventional top-K
+ * routing almost always above zero; MoGE's group top-K' keeps it at zero).
+ * For every batch b in [0, batches) of cfg->T tokens and cfg->N experts the
+ * call draws scores on the device,
+ *   s[b,t,e] = z((b*T + t)*N + e) + bias[e]     (bias may be NULL = 0),
+ * where z(i) is an Irwin-Hall approximation of N(0,1): the twelve 16-bit fields
+ * u of the splitmix64 words mix(key + 3i), mix(key + 3i + 1), mix(key + 3i + 2),
+ * key = mix(seed XOR 8), give z = sum (u + 1/2) / 2^16 - 6 (exact in fp32).
+ * Each token is routed both ways on its fp32 scores (group top-K' as in
+ * moge_route(MOGE_ROUTE_GROUPED), and top-K over all N with K = M*K'; ties go to
+ * the lower index), and the groups of the selected experts are counted:
+ *   loads_grouped[b*M + g], loads_global[b*M + g]   (int32, outputs, required)
+ *   is_grouped[b], is_global[b] = (max_g load - min_g load) / T  (fp32, or NULL)
+ * Only T, N, M and k_per_group of cfg are used; N <= 256.  Allocates nothing;
+ * the load arrays are zeroed by the call.  Exact and reproducible (integer
+ * counts). */
+moge_status_t moge_imbalance_study(const moge_config_t *cfg, int64_t batches, uint64_t seed, const float *bias,
+                                   int32_t *loads_grouped, int32_t *loads_global, float *is_grouped,
+                                   float *is_global, moge_stream_t stream);
+
 /* ---- Instrumentation (no counterpart on the pages: measurement support) ---- */
 
 /* Stages of moge_layer_forward, in launch order. */

@@ -74,9 +74,10 @@ def load():
         lib.moge_layer_forward.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Aux), vp, sz, vp]
         lib.moge_permute_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.moge_permute_noalloc.restype = i32
+        lib.moge_imbalance_study.argtypes = [cfgp, ctypes.c_int64, ctypes.c_uint64, vp, vp, vp, vp, vp, vp]
         lib.moge_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         lib.moge_kernel_launch_count.restype = ctypes.c_uint64
-        for fn in ("moge_set_stage_events", "moge_reset_device_status", "moge_query_device_status", "moge_route", "moge_permute",
+        for fn in ("moge_imbalance_study", "moge_set_stage_events", "moge_reset_device_status", "moge_query_device_status", "moge_route", "moge_permute",
                    "moge_expert_ffn", "moge_combine", "moge_imbalance_score", "moge_layer_forward"):
             getattr(lib, fn).restype = i32
         _lib = lib
@@ -206,6 +207,13 @@ def moge_set_stage_events(events) -> None:
 
 
 _stage_array = None
+
+
+def moge_imbalance_study(cfg, batches, seed, bias, loads_grouped, loads_global, is_grouped=None, is_global=None,
+                         stream=None) -> None:
+    _check("moge_imbalance_study", load().moge_imbalance_study(
+        ctypes.byref(cfg), int(batches), int(seed), _ptr(bias), _ptr(loads_grouped), _ptr(loads_global),
+        _ptr(is_grouped), _ptr(is_global), _stream(stream)))
 
 
 def moge_kernel_launch_count() -> int:

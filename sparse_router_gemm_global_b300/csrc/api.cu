@@ -295,6 +295,23 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
     return cuda_status(e);
 }
 
+moge_status_t moge_imbalance_study(const moge_config_t *cfg, int64_t batches, uint64_t seed, const float *bias,
+                                   int32_t *loads_grouped, int32_t *loads_global, float *is_grouped,
+                                   float *is_global, moge_stream_t stream) {
+    moge_status_t s = check_routing(cfg);
+    if (s != MOGE_OK) return s;
+    if (batches < 0 || !loads_grouped || !loads_global) return MOGE_ERR_INVALID_ARGUMENT;
+    for (const void *p : {(const void *)bias, (const void *)loads_grouped, (const void *)loads_global,
+                          (const void *)is_grouped, (const void *)is_global})
+        if (p && !aligned16(p)) return MOGE_ERR_INVALID_ARGUMENT;
+    if (cfg->N > kStudyMaxExperts || cfg->T > (1 << 30) || batches * cfg->M > ((int64_t)1 << 31) ||
+        imbalance_study_smem_bytes(cfg->N, cfg->M) > 200 * 1024)
+        return MOGE_ERR_UNSUPPORTED;
+    return cuda_status(launch_imbalance_study(cfg->T, cfg->N, cfg->M, cfg->k_per_group, batches, seed, bias,
+                                              loads_grouped, loads_global, is_grouped, is_global,
+                                              (cudaStream_t)stream));
+}
+
 moge_status_t moge_set_stage_events(void *const *events, int n) {
     if (events && n != MOGE_NUM_STAGES + 1) return MOGE_ERR_INVALID_ARGUMENT;
     t_stage_events = events;

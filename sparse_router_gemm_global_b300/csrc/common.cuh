@@ -131,6 +131,12 @@ cudaError_t launch_route_small(const void *x, const void *w_r, const float *bias
                                int32_t *idx, float *gate, uint32_t *ticket, uint32_t *status, int32_t *counts,
                                int32_t *offsets, int32_t *pair_row, int32_t *row_token, int32_t *group_load,
                                float *score, cudaStream_t s);
+// Monte-Carlo imbalance study (imbalance_study.cu): N <= kStudyMaxExperts.
+constexpr int64_t kStudyMaxExperts = 256;
+size_t imbalance_study_smem_bytes(int64_t N, int64_t M);
+cudaError_t launch_imbalance_study(int64_t T, int64_t N, int64_t M, int64_t kpg, int64_t batches, uint64_t seed,
+                                   const float *bias, int32_t *loads_grouped, int32_t *loads_global,
+                                   float *is_grouped, float *is_global, cudaStream_t s);
 cudaError_t launch_router_logits_simt(const void *x, const void *w_r, const float *bias, int64_t T,
                                       int64_t d, int64_t N, int dtype, float *logits, cudaStream_t s);
 cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, int32_t *counts,

@@ -127,12 +127,25 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
 // ---------------------------------------------------------------------------------------------
 // Row gather x_perm[r,:] = x[row_token[r],:]; one warp per row, 16-byte vectors, each lane
 // issuing 8 loads before their stores so that a row's reads are in flight together.
-// Only rows r < offsets[N] (the pairs that exist) are copied.
+// Only rows r < offsets[N] (the pairs that exist) are copied.  Every row of x is read once per
+// expert its token selected, so x is loaded with an evict-last L2 policy and x_perm (written
+// once, read back much later) is stored with the streaming hint: the copy then moves about one
+// pass of x_perm through HBM instead of also re-reading x.
 // ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ int4 ld_keep(const int4 *p, uint64_t pol) {
+    int4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.s32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 __global__ void gather_rows_kernel(const int4 *__restrict__ x, const int32_t *__restrict__ row_token,
                                    const int32_t *__restrict__ offsets, int N, int64_t vec_per_row,
                                    int4 *__restrict__ x_perm) {
     constexpr int kBatch = 8;
+    uint64_t keep;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
     const int64_t rows = offsets[N];
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -146,12 +159,12 @@ __global__ void gather_rows_kernel(const int4 *__restrict__ x, const int32_t *__
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
                 const int64_t v = v0 + 32 * j;
-                if (v < vec_per_row) buf[j] = __ldg(src + v);
+                if (v < vec_per_row) buf[j] = ld_keep(src + v, keep);
             }
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
                 const int64_t v = v0 + 32 * j;
-                if (v < vec_per_row) dst[v] = buf[j];
+                if (v < vec_per_row) __stcs(dst + v, buf[j]);
             }
         }
     }

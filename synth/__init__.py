@@ -17,6 +17,8 @@ Tensor ids (one independent stream each):
  5    W_down       [N, d, I]     N(0, 1/I)
  6    rank perm    [N]           Fisher-Yates permutation of 1..N
  7    logit noise  [T, N]        N(0, 1) (routing-only workload)
+ 8    study scores [B, T, N]     Irwin-Hall(12) ~ N(0, 1), bit-exact by construction
+                                 (imbalance Monte-Carlo study; see synth.c)
 ====  =====================================================
 """
 from __future__ import annotations
@@ -36,7 +38,7 @@ _LIB_PATH = os.path.join(_HERE, "libsynth.so")
 _lock = threading.Lock()
 _lib = None
 
-TID_X, TID_WR, TID_WGATE, TID_WUP, TID_WDOWN, TID_RANK, TID_LOGIT_NOISE = 1, 2, 3, 4, 5, 6, 7
+TID_X, TID_WR, TID_WGATE, TID_WUP, TID_WDOWN, TID_RANK, TID_LOGIT_NOISE, TID_STUDY = 1, 2, 3, 4, 5, 6, 7, 8
 BIAS_SCALE = 1.5
 
 
@@ -64,6 +66,7 @@ def _get():
             lib.synth_f32_to_bf16.argtypes = [vp, u64, vp]
             lib.synth_rank_permutation.argtypes = [u64, u64, i64, vp]
             lib.synth_rank_bias.argtypes = [vp, i64, dbl, vp]
+            lib.synth_study_scores.argtypes = [u64, u64, i64, i64, i64, i64, vp]
             lib.synth_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -149,3 +152,12 @@ def expert_weights(w: "Workload", e: int, seed: int = DEFAULT_SEED) -> tuple:
     return (normal(seed, TID_WGATE, (I, d), d ** -0.5, dt, start=e * blk),
             normal(seed, TID_WUP, (I, d), d ** -0.5, dt, start=e * blk),
             normal(seed, TID_WDOWN, (d, I), I ** -0.5, dt, start=e * blk))
+
+
+def study_scores(seed: int, b0: int, nb: int, T: int, N: int) -> np.ndarray:
+    """Noise of batches [b0, b0+nb) of the imbalance Monte-Carlo study, [nb, T, N] fp32
+    (Irwin-Hall sum of twelve 16-bit uniforms minus 6; exact, see synth.c).  The study's
+    scores are this noise plus the router bias, one fp32 addition."""
+    out = np.empty((nb, T, N), dtype=np.float32)
+    _get().synth_study_scores(seed, TID_STUDY, b0, nb, T, N, out.ctypes.data)
+    return out

@@ -113,6 +113,30 @@ void synth_rank_bias(const int32_t *rank, int64_t n, double scale, float *bias) 
     for (int64_t i = 0; i < n; ++i) bias[i] = (float)(scale * log(1.0 / (double)rank[i]));
 }
 
+/* Scores of the imbalance Monte-Carlo study: element i of the stream (i = (b*T + t)*N + e for
+ * batch b, token t, expert e) is an Irwin-Hall approximation of N(0,1) built from three words,
+ *   words w_j = word(3i + j), j = 0..2;  S = sum of the twelve 16-bit fields of w_0..w_2;
+ *   z = (2S + 12) / 2^17 - 6  ( = sum of twelve uniforms (u + 1/2)/2^16, minus 6 ).
+ * Every step is exact in fp32 (2S + 12 < 2^21), so any implementation of this definition
+ * produces the same bits.  Writes batches [b0, b0 + nb) as [nb][T][N]. */
+void synth_study_scores(uint64_t seed, uint64_t tensor_id, int64_t b0, int64_t nb, int64_t T, int64_t N,
+                        float *out) {
+    const uint64_t key = stream_key(seed, tensor_id);
+    const int64_t n = nb * T * N;
+    const uint64_t first = (uint64_t)b0 * (uint64_t)T * (uint64_t)N;
+#pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < n; ++k) {
+        const uint64_t i = first + (uint64_t)k;
+        uint32_t S = 0;
+        for (int j = 0; j < 3; ++j) {
+            const uint64_t w = mix64(key + 3 * i + (uint64_t)j);
+            S += (uint32_t)(w & 0xFFFFu) + (uint32_t)((w >> 16) & 0xFFFFu) + (uint32_t)((w >> 32) & 0xFFFFu) +
+                 (uint32_t)(w >> 48);
+        }
+        out[k] = (float)(2u * S + 12u) * (1.0f / 131072.0f) - 6.0f;
+    }
+}
+
 int synth_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

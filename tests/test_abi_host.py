@@ -117,3 +117,17 @@ def test_routing_only_config_needs_no_hidden_size():
     lib = binding.load()
     # logits-input routing validates without d / I; fails here only on the workspace size
     assert lib.moge_route(ctypes.byref(c), 0, None, None, None, FAKE, FAKE, FAKE, FAKE, 64, None) == WORKSPACE
+
+
+def test_imbalance_study_rejects_bad_arguments():
+    lib = binding.load()
+    f = lib.moge_imbalance_study
+    c = cfg(T=64, N=16, M=4, kpg=1)
+    assert f(ctypes.byref(c), 4, 1, None, None, FAKE, None, None, None) == INVALID      # loads required
+    assert f(ctypes.byref(c), -1, 1, None, FAKE, FAKE, None, None, None) == INVALID     # batches < 0
+    assert f(ctypes.byref(c), 4, 1, None, FAKE + 4, FAKE, None, None, None) == INVALID  # misaligned
+    wide = cfg(T=64, N=512, M=4, kpg=1)
+    assert f(ctypes.byref(wide), 4, 1, None, FAKE, FAKE, None, None, None) == UNSUPPORTED
+    bad = cfg(T=64, N=15, M=4, kpg=1)
+    assert f(ctypes.byref(bad), 4, 1, None, FAKE, FAKE, None, None, None) == INVALID
+    assert f(None, 4, 1, None, FAKE, FAKE, None, None, None) == INVALID
