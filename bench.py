@@ -38,6 +38,7 @@ PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SRC = os.path.join(ROOT, "sparse_router_gemm_global_b300", "csrc", "ffn_tc.cu")
+SHARED_EXPERTS = 4   # Pangu Pro MoE: 64 routed + 4 shared experts (explainer, section 2)
 
 
 # --------------------------------------------------------------------------------------------
@@ -169,14 +170,15 @@ def upload(inp, device):
 
 
 class Layer:
-    """Device buffers of one workload and the C-ABI call of one step."""
+    """Device buffers of one workload and the C-ABI call of one step (with n_shared shared experts
+    when n_shared > 0; the weight tensors then hold N + n_shared experts)."""
 
-    def __init__(self, w, d_inp, device):
+    def __init__(self, w, d_inp, device, n_shared=0):
         import torch
         import sparse_router_gemm_global_b300 as moge
-        self.moge, self.w, self.dev = moge, w, device
+        self.moge, self.w, self.dev, self.n_shared = moge, w, device, n_shared
         self.cfg = moge.make_config(w.T, w.d, w.N, w.M, w.kpg, w.I, w.dtype)
-        self.ws = moge.alloc_workspace(self.cfg, device)
+        self.ws = moge.alloc_workspace(self.cfg, device, n_shared=n_shared)
         self.d = d_inp
         self.x = d_inp["x"][: w.T].contiguous()
         self.y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=device)
@@ -186,8 +188,14 @@ class Layer:
 
     def step(self, x=None, y=None):
         d = self.d
-        self.moge.moge_layer_forward(self.cfg, self.x if x is None else x, d["w_router"], d["bias"], d["w_gate"],
-                                     d["w_up"], d["w_down"], self.y if y is None else y, self.ws, aux=self.aux)
+        x = self.x if x is None else x
+        y = self.y if y is None else y
+        if self.n_shared:
+            self.moge.moge_layer_forward_shared(self.cfg, self.n_shared, x, d["w_router"], d["bias"], d["w_gate"],
+                                                d["w_up"], d["w_down"], y, self.ws, aux=self.aux)
+        else:
+            self.moge.moge_layer_forward(self.cfg, x, d["w_router"], d["bias"], d["w_gate"], d["w_up"],
+                                         d["w_down"], y, self.ws, aux=self.aux)
 
 
 def timed_steps(layer, steps, warmup, dist, clock=None):
@@ -312,6 +320,35 @@ def e2e_steps(layer, steps, dist):
     return ms, x_host[0].numel() * 2, y_host[0].numel() * 2
 
 
+def imbalance_study(batches, device):
+    """moge_imbalance_study over `batches` batches of the routing workload's shape (T=16384,
+    N=64 in 8 groups, K'=2, the same popularity bias): device time and the distribution of the
+    imbalance score for MoGE and for global top-16."""
+    import torch
+    import sparse_router_gemm_global_b300 as moge
+    w = WORKLOADS["routing_16k"]
+    c = moge.make_config(w.T, 0, w.N, w.M, w.kpg, 0, "f32")
+    bias = torch.from_numpy(synth.router_bias(DEFAULT_SEED, w.N)).to(device)
+    lg = torch.empty((batches, w.M), dtype=torch.int32, device=device)
+    lc = torch.empty_like(lg)
+    ig = torch.empty(batches, dtype=torch.float32, device=device)
+    ic = torch.empty_like(ig)
+    moge.moge_imbalance_study(c, batches, DEFAULT_SEED, bias, lg, lc, ig, ic)  # warm-up
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    moge.moge_imbalance_study(c, batches, DEFAULT_SEED, bias, lg, lc, ig, ic)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e)
+    g, glob = ig.cpu().numpy(), ic.cpu().numpy()
+    return {"workload": f"{w.name} x {batches} batches", "batches": batches, "ms": round(ms, 3),
+            "tokens_per_s": round(batches * w.T / (ms / 1e3), 1),
+            "moge": {"mean": float(g.mean()), "max": float(g.max())},
+            "global_topk": {"mean": round(float(glob.mean()), 4), "min": round(float(glob.min()), 4),
+                            "max": round(float(glob.max()), 4), "frac_above_zero": float((glob > 0).mean())}}
+
+
 def gate_up_roofline(w, counts, stage_ms, pk, peak_kind):
     """Roofline of the dominant kernel (grouped gate/up GEMM + SwiGLU) from its stage time."""
     P = w.P
@@ -391,7 +428,9 @@ def run_ours(args):
     if args.tokens:  # a smaller token count of the same layer (profiling captures)
         wp = wp.with_(name=f"{wp.name}[T={args.tokens}]", T=args.tokens)
     wd = WORKLOADS["decode_t32"]
-    inp = synth.layer_inputs(wp, seed=DEFAULT_SEED)   # decode reuses the same weights and the first 32 tokens
+    # decode reuses the same weights and the first 32 tokens; the weight tensors also hold the
+    # shared experts of the shared-expert measurement (the routed layer reads the first N)
+    inp = synth.layer_inputs(wp, seed=DEFAULT_SEED, n_shared=SHARED_EXPERTS)
     d_inp = upload(inp, device)
 
     prefill = Layer(wp, d_inp, device)
@@ -417,6 +456,24 @@ def run_ours(args):
                   "roofline": gate_up_roofline(wd, dcounts, dgate_up_ms, pk, peak_kind),
                   "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
                   "stage_ms": dstages, "gpu_launches": int(dlaunches)}
+
+    # the same layers with Pangu Pro's 4 shared experts added (every token visits each of them)
+    shared = None
+    if args.shared_steps > 0:
+        shared = {"n_shared": SHARED_EXPERTS}
+        for name, w, n in (("prefill", wp, args.shared_steps), ("decode", wd, 3 * args.shared_steps)):
+            L = Layer(w, d_inp, device, n_shared=SHARED_EXPERTS)
+            sms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist)
+            rows = w.P + SHARED_EXPERTS * w.T
+            shared[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "value": round(w.T * ws_n / (sms / 1e3), 1),
+                            "unit": "tokens/s", "ms_per_step": round(sms, 4), "steps": n,
+                            "tflops": round(6.0 * rows * w.d * w.I / (sms / 1e3) / 1e12, 2)}
+            del L
+
+    # Monte-Carlo imbalance study on the routing workload's shape (MoGE vs global top-K)
+    study = None
+    if args.study_batches > 0:
+        study = imbalance_study(args.study_batches, device)
 
     # end to end through the public call with host buffers
     e2e = None
@@ -452,6 +509,8 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": int(launches),
         "decode": decode,
+        "shared_experts": shared,
+        "imbalance_study": study,
     }
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wp, inp, budget_s=args.cpu_budget)
@@ -552,6 +611,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_t8192", choices=["prefill_t8192"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
+    ap.add_argument("--shared-steps", type=int, default=50, help="steps of the shared-expert layers (0: skip)")
+    ap.add_argument("--study-batches", type=int, default=1000, help="Monte-Carlo study batches (0: skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle FFN work")

@@ -205,6 +205,23 @@ moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const 
                                  const void *w_down, void *y, const moge_aux_t *aux, void *ws,
                                  size_t ws_bytes, moge_stream_t stream);
 
+/* The layer with S = n_shared shared experts in addition to the N routed ones
+ * (the Pangu Pro MoE explainer, section 2 "hardware co-design", gives the model
+ * 64 routed and 4 shared experts; the pages say no more about them).  Reading
+ * taken: every token visits every shared expert, each a SwiGLU FFN of the same
+ * shape as a routed expert, and their outputs are added with weight 1:
+ *   y[t] = sum_k gate[t,k] FFN_{idx[t,k]}(x[t]) + sum_{s<S} FFN_{N+s}(x[t]).
+ * w_gate, w_up [N+S,I,d] and w_down [N+S,d,I] hold the routed experts first and
+ * the shared ones after them.  Routing, aux outputs (aux->offsets: the N+1
+ * routed offsets) and errors are those of moge_layer_forward; 0 <= n_shared <= 64
+ * and N + n_shared <= 1024.  Needs moge_workspace_bytes_shared(cfg, n_shared)
+ * bytes of workspace (0 when cfg or n_shared is invalid). */
+size_t moge_workspace_bytes_shared(const moge_config_t *cfg, int64_t n_shared);
+moge_status_t moge_layer_forward_shared(const moge_config_t *cfg, int64_t n_shared, const void *x,
+                                        const void *w_router, const float *bias, const void *w_gate,
+                                        const void *w_up, const void *w_down, void *y, const moge_aux_t *aux,
+                                        void *ws, size_t ws_bytes, moge_stream_t stream);
+
 /* Monte-Carlo study of the imbalance score (Pangu Pro MoE explainer, section 1:
  * a Monte-Carlo simulation finds the imbalance score of conventional top-K
  * routing almost always above zero; MoGE's group top-K' keeps it at zero).

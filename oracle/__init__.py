@@ -200,6 +200,19 @@ def combine_tokens(tokens, idx, gate64, x, w_gate, w_up, w_down) -> np.ndarray:
     return y
 
 
+def shared_experts_tokens(tokens, n_routed: int, n_shared: int, x, w_gate, w_up, w_down) -> np.ndarray:
+    """[n, d] float64: sum over the shared experts s = 0..S-1 (weights at index N + s) of their
+    SwiGLU FFN on each listed token, weight 1.  The explainer's section 2 gives Pangu Pro MoE 4
+    shared experts beside the 64 routed ones and nothing more; the reading taken is that every
+    token visits every shared expert and their outputs are added to the routed combine."""
+    tokens = _c(tokens, np.int32)
+    out = np.zeros((tokens.shape[0], x.shape[1]), dtype=np.float64)
+    for s in range(n_shared):
+        out += expert_ffn_pairs(tokens, np.full(tokens.shape[0], n_routed + s, dtype=np.int32), x, w_gate, w_up,
+                                w_down)
+    return out
+
+
 def combine_rows(rows, pair_row, gate64) -> np.ndarray:
     """y [T, d] float64 = sum_k gate[t,k] * rows[pair_row[t,k]] (the combine step alone)."""
     dt = _dt(rows)
@@ -230,13 +243,15 @@ def route(logits, M: int, kpg: int, mode: str = "grouped") -> dict:
 
 
 def layer_forward(x, w_router, bias, w_gate, w_up, w_down, M: int, kpg: int, tokens=None,
-                  logits=None) -> dict:
+                  logits=None, n_shared: int = 0) -> dict:
     """The whole MoGE layer for the listed tokens (all tokens if None).
 
     Routing is computed for every token (the permutation and the loads need
     all of them); the expert FFN and combine only for ``tokens``.  Passing
     ``logits`` replaces the router projection by those scores (used to
-    re-run the FFN under another routing).
+    re-run the FFN under another routing).  With ``n_shared`` > 0 the weight
+    arrays hold N + n_shared experts and the shared experts' outputs are added
+    (see shared_experts_tokens).
     """
     if logits is None:
         logits = router_logits(x, w_router, bias)
@@ -246,4 +261,6 @@ def layer_forward(x, w_router, bias, w_gate, w_up, w_down, M: int, kpg: int, tok
         tokens = np.arange(T, dtype=np.int32)
     r["tokens"] = np.asarray(tokens, dtype=np.int32)
     r["y"] = combine_tokens(r["tokens"], r["idx"], r["gate64"], x, w_gate, w_up, w_down)
+    if n_shared:
+        r["y"] = r["y"] + shared_experts_tokens(r["tokens"], w_router.shape[0], n_shared, x, w_gate, w_up, w_down)
     return r

@@ -74,10 +74,14 @@ def load():
         lib.moge_layer_forward.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Aux), vp, sz, vp]
         lib.moge_permute_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.moge_permute_noalloc.restype = i32
+        lib.moge_workspace_bytes_shared.restype = sz
+        lib.moge_workspace_bytes_shared.argtypes = [cfgp, ctypes.c_int64]
+        lib.moge_layer_forward_shared.argtypes = [cfgp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp,
+                                                  ctypes.POINTER(Aux), vp, sz, vp]
         lib.moge_imbalance_study.argtypes = [cfgp, ctypes.c_int64, ctypes.c_uint64, vp, vp, vp, vp, vp, vp]
         lib.moge_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         lib.moge_kernel_launch_count.restype = ctypes.c_uint64
-        for fn in ("moge_imbalance_study", "moge_set_stage_events", "moge_reset_device_status", "moge_query_device_status", "moge_route", "moge_permute",
+        for fn in ("moge_layer_forward_shared", "moge_imbalance_study", "moge_set_stage_events", "moge_reset_device_status", "moge_query_device_status", "moge_route", "moge_permute",
                    "moge_expert_ffn", "moge_combine", "moge_imbalance_score", "moge_layer_forward"):
             getattr(lib, fn).restype = i32
         _lib = lib
@@ -122,10 +126,15 @@ def moge_workspace_bytes(cfg: Config) -> int:
     return load().moge_workspace_bytes(ctypes.byref(cfg))
 
 
-def alloc_workspace(cfg: Config, device="cuda"):
-    """A device workspace of moge_workspace_bytes(cfg) bytes with its status word cleared."""
+def moge_workspace_bytes_shared(cfg: Config, n_shared: int) -> int:
+    return load().moge_workspace_bytes_shared(ctypes.byref(cfg), int(n_shared))
+
+
+def alloc_workspace(cfg: Config, device="cuda", n_shared: int = 0):
+    """A device workspace of moge_workspace_bytes(cfg) bytes (moge_workspace_bytes_shared with
+    n_shared > 0) with its status word cleared."""
     import torch
-    n = moge_workspace_bytes(cfg)
+    n = moge_workspace_bytes_shared(cfg, n_shared) if n_shared else moge_workspace_bytes(cfg)
     if n == 0:
         raise MoGEError("moge_workspace_bytes", 1)
     ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -226,3 +235,11 @@ def moge_layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, y, ws, aux:
     _check("moge_layer_forward", load().moge_layer_forward(
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(y),
         ctypes.byref(a), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moge_layer_forward_shared(cfg, n_shared, x, w_router, bias, w_gate, w_up, w_down, y, ws,
+                              aux: dict | None = None, stream=None) -> None:
+    a = Aux(*[_ptr((aux or {}).get(k)) for k, _ in Aux._fields_])
+    _check("moge_layer_forward_shared", load().moge_layer_forward_shared(
+        ctypes.byref(cfg), int(n_shared), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate), _ptr(w_up),
+        _ptr(w_down), _ptr(y), ctypes.byref(a), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))

@@ -61,11 +61,13 @@ moge_status_t check_layer(const moge_config_t *c) {
     return MOGE_OK;
 }
 
-moge_status_t check_ws(const moge_config_t *c, void *ws, size_t ws_bytes) {
+moge_status_t check_ws(const moge_config_t *c, void *ws, size_t ws_bytes, int64_t S = 0) {
     if (!ws || ((uintptr_t)ws & 255u) != 0) return MOGE_ERR_WORKSPACE;
-    if (ws_bytes < ws_layout(*c).total) return MOGE_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(*c, S).total) return MOGE_ERR_WORKSPACE;
     return MOGE_OK;
 }
+
+constexpr int64_t kMaxShared = 64;
 
 template <typename T> T *at(void *ws, size_t off) { return (T *)((char *)ws + off); }
 
@@ -95,19 +97,103 @@ moge_status_t route_impl(const moge_config_t *c, moge_route_mode_t mode, const v
                                            mode == MOGE_ROUTE_GLOBAL_TOPK, idx, gate, st));
 }
 
-// act = x_perm (row_token == nullptr) or x gathered through row_token (bf16 only).
+// act = x_perm (row_token == nullptr) or x gathered through row_token (bf16 only).  With S shared
+// experts the expert index space is N + S and the rows P + S*T.
 moge_status_t ffn_impl(const moge_config_t *c, const void *act, const int32_t *row_token, const int32_t *offsets,
-                       const void *wg, const void *wu, const void *wd, void *y_perm, void *ws, cudaStream_t st) {
-    const WsLayout L = ws_layout(*c);
-    const int64_t P = c->T * c->M * c->k_per_group;
+                       const void *wg, const void *wu, const void *wd, void *y_perm, void *ws, cudaStream_t st,
+                       int64_t S = 0) {
+    const WsLayout L = ws_layout(*c, S);
+    const int64_t rows = c->T * c->M * c->k_per_group + S * c->T;
+    const int64_t experts = c->N + S;
     void *h = at<void>(ws, L.h);
     uint32_t *status = at<uint32_t>(ws, L.status);
     if (c->act_dtype == MOGE_BF16)
-        return cuda_status(launch_ffn_tc(act, row_token, offsets, c->N, P, c->T, c->d, c->I, wg, wu, wd, h, y_perm,
-                                         status, st));
+        return cuda_status(launch_ffn_tc(act, row_token, offsets, experts, rows, c->T, c->d, c->I, wg, wu, wd, h,
+                                         y_perm, status, st));
     const void *x_perm = act;
-    return cuda_status(launch_ffn_simt(x_perm, offsets, c->N, P, c->d, c->I, c->act_dtype, wg, wu, wd, h,
+    return cuda_status(launch_ffn_simt(x_perm, offsets, experts, rows, c->d, c->I, c->act_dtype, wg, wu, wd, h,
                                        y_perm, st));
+}
+
+// The whole layer with S >= 0 shared experts (weights of N + S experts; S = 0 is the MoGE layer).
+moge_status_t layer_impl(const moge_config_t *cfg, int64_t S, const void *x, const void *w_router,
+                         const float *bias, const void *w_gate, const void *w_up, const void *w_down, void *y,
+                         const moge_aux_t *aux, void *ws, size_t ws_bytes, moge_stream_t stream) {
+    moge_status_t s = check_layer(cfg);
+    if (s != MOGE_OK) return s;
+    if (S < 0 || S > kMaxShared) return MOGE_ERR_INVALID_ARGUMENT;
+    if (cfg->N + S > kMaxExperts) return MOGE_ERR_UNSUPPORTED;
+    if (!w_router || !w_gate || !w_up || !w_down) return MOGE_ERR_INVALID_ARGUMENT;
+    if (cfg->T > 0 && (!x || !y)) return MOGE_ERR_INVALID_ARGUMENT;  // an empty batch may pass NULL
+    moge_aux_t a = aux ? *aux : moge_aux_t{};
+    for (const void *p : {x, w_router, (const void *)bias, w_gate, w_up, w_down, (const void *)y,
+                          (const void *)a.logits, (const void *)a.topk_idx, (const void *)a.topk_gate,
+                          (const void *)a.counts, (const void *)a.offsets, (const void *)a.group_load,
+                          (const void *)a.score})
+        if (p && !aligned16(p)) return MOGE_ERR_INVALID_ARGUMENT;
+    if ((s = check_ws(cfg, ws, ws_bytes, S)) != MOGE_OK) return s;
+    const WsLayout L = ws_layout(*cfg, S);
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t K = cfg->M * cfg->k_per_group;
+    const int64_t P = cfg->T * K;
+    const int64_t rows = P + S * cfg->T;
+    if (cfg->T == 0) {  // empty batch: only the counts/offsets/score outputs exist
+        if (a.counts || a.offsets || a.score || a.group_load) {
+            int32_t *counts = a.counts ? a.counts : at<int32_t>(ws, L.counts);
+            int32_t *offsets = a.offsets ? a.offsets : at<int32_t>(ws, L.offsets);
+            return cuda_status(launch_permute(nullptr, 0, K, cfg->N, counts, offsets, nullptr, nullptr, nullptr,
+                                              nullptr, st, cfg->M, a.group_load, a.score));
+        }
+        return MOGE_OK;
+    }
+    int32_t *idx = a.topk_idx ? a.topk_idx : at<int32_t>(ws, L.idx);
+    float *gate = a.topk_gate ? a.topk_gate : at<float>(ws, L.gate);
+    int32_t *counts = a.counts ? a.counts : at<int32_t>(ws, L.counts);
+    // the expert offsets live in the workspace whenever shared experts extend them past N + 1
+    int32_t *offsets = (a.offsets && S == 0) ? a.offsets : at<int32_t>(ws, L.offsets);
+    int32_t *pair_row = at<int32_t>(ws, L.pair_row);
+    int32_t *row_token = at<int32_t>(ws, L.row_token);
+    void *x_perm = at<void>(ws, L.x_perm);
+    void *y_perm = at<void>(ws, L.y_perm);
+
+    mark_stage(MOGE_STAGE_ROUTE, st);
+    cudaError_t e = cudaSuccess;
+    if (route_small_fits(cfg->T, cfg->N, K, cfg->M, true)) {
+        // few tokens: routing and permutation in one launch; the permutation stage is empty
+        e = launch_route_small(x, w_router, bias, cfg->T, cfg->d, cfg->N, cfg->M, cfg->k_per_group, false,
+                               cfg->act_dtype, at<float>(ws, L.logits), a.logits, idx, gate,
+                               at<uint32_t>(ws, kTicketOffset), at<uint32_t>(ws, L.status), counts, offsets,
+                               pair_row, row_token, a.group_load, a.score, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        mark_stage(MOGE_STAGE_PERMUTE, st);
+    } else {
+        if ((s = route_impl(cfg, MOGE_ROUTE_GROUPED, x, w_router, bias, a.logits, idx, gate, ws, st)) != MOGE_OK)
+            return s;
+        mark_stage(MOGE_STAGE_PERMUTE, st);  // the permutation also writes the imbalance outputs
+        e = launch_permute(idx, cfg->T, K, cfg->N, counts, offsets, pair_row, row_token,
+                           at<int32_t>(ws, L.chunk_counts), at<uint32_t>(ws, L.status), st, cfg->M, a.group_load,
+                           a.score);
+    }
+    if (e == cudaSuccess) e = launch_shared_rows(cfg->T, cfg->N, S, P, offsets, row_token, st);
+    if (e == cudaSuccess && a.offsets && S > 0)
+        e = cudaMemcpyAsync(a.offsets, offsets, (size_t)(cfg->N + 1) * 4, cudaMemcpyDeviceToDevice, st);
+    // bf16: the gate/up GEMM gathers the token rows itself at T <= 64 (weights-as-M tiles, TMA
+    // gather4 through row_token) and the gather stage is empty; otherwise rows are first copied to
+    // x_perm and loaded as tiles.
+    const bool gather_in_gemm = gathers_in_gemm(*cfg);
+    mark_stage(MOGE_STAGE_GATHER, st);
+    if (e == cudaSuccess && !gather_in_gemm)
+        e = launch_gather_rows(x, row_token, offsets, cfg->N + S, rows, cfg->d, cfg->act_dtype, x_perm, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    mark_stage(MOGE_STAGE_GATE_UP, st);  // the FFN marks MOGE_STAGE_DOWN between its two GEMMs
+    s = gather_in_gemm ? ffn_impl(cfg, x, row_token, offsets, w_gate, w_up, w_down, y_perm, ws, st, S)
+                       : ffn_impl(cfg, x_perm, nullptr, offsets, w_gate, w_up, w_down, y_perm, ws, st, S);
+    if (s != MOGE_OK) return s;
+    mark_stage(MOGE_STAGE_COMBINE, st);
+    e = launch_combine(y_perm, pair_row, gate, cfg->T, K, cfg->d, cfg->act_dtype, y, st, S, P);
+    mark_stage(MOGE_STAGE_IMBALANCE, st);  // empty: computed with the permutation
+    mark_stage(MOGE_NUM_STAGES, st);
+    return cuda_status(e);
 }
 
 }  // namespace
@@ -225,74 +311,22 @@ moge_status_t moge_imbalance_score(const moge_config_t *cfg, const int32_t *coun
 moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const void *w_router, const float *bias,
                                  const void *w_gate, const void *w_up, const void *w_down, void *y,
                                  const moge_aux_t *aux, void *ws, size_t ws_bytes, moge_stream_t stream) {
-    moge_status_t s = check_layer(cfg);
-    if (s != MOGE_OK) return s;
-    if (!w_router || !w_gate || !w_up || !w_down) return MOGE_ERR_INVALID_ARGUMENT;
-    if (cfg->T > 0 && (!x || !y)) return MOGE_ERR_INVALID_ARGUMENT;  // an empty batch may pass NULL
-    moge_aux_t a = aux ? *aux : moge_aux_t{};
-    for (const void *p : {x, w_router, (const void *)bias, w_gate, w_up, w_down, (const void *)y,
-                          (const void *)a.logits, (const void *)a.topk_idx, (const void *)a.topk_gate,
-                          (const void *)a.counts, (const void *)a.offsets, (const void *)a.group_load,
-                          (const void *)a.score})
-        if (p && !aligned16(p)) return MOGE_ERR_INVALID_ARGUMENT;
-    if ((s = check_ws(cfg, ws, ws_bytes)) != MOGE_OK) return s;
-    const WsLayout L = ws_layout(*cfg);
-    cudaStream_t st = (cudaStream_t)stream;
-    const int64_t K = cfg->M * cfg->k_per_group;
-    const int64_t P = cfg->T * K;
-    if (cfg->T == 0) {  // empty batch: only the counts/offsets/score outputs exist
-        if (a.counts || a.offsets || a.score || a.group_load) {
-            int32_t *counts = a.counts ? a.counts : at<int32_t>(ws, L.counts);
-            int32_t *offsets = a.offsets ? a.offsets : at<int32_t>(ws, L.offsets);
-            return cuda_status(launch_permute(nullptr, 0, K, cfg->N, counts, offsets, nullptr, nullptr, nullptr,
-                                              nullptr, st, cfg->M, a.group_load, a.score));
-        }
-        return MOGE_OK;
-    }
-    int32_t *idx = a.topk_idx ? a.topk_idx : at<int32_t>(ws, L.idx);
-    float *gate = a.topk_gate ? a.topk_gate : at<float>(ws, L.gate);
-    int32_t *counts = a.counts ? a.counts : at<int32_t>(ws, L.counts);
-    int32_t *offsets = a.offsets ? a.offsets : at<int32_t>(ws, L.offsets);
-    int32_t *pair_row = at<int32_t>(ws, L.pair_row);
-    int32_t *row_token = at<int32_t>(ws, L.row_token);
-    void *x_perm = at<void>(ws, L.x_perm);
-    void *y_perm = at<void>(ws, L.y_perm);
+    return layer_impl(cfg, 0, x, w_router, bias, w_gate, w_up, w_down, y, aux, ws, ws_bytes, stream);
+}
 
-    mark_stage(MOGE_STAGE_ROUTE, st);
-    cudaError_t e = cudaSuccess;
-    if (route_small_fits(cfg->T, cfg->N, K, cfg->M, true)) {
-        // few tokens: routing and permutation in one launch; the permutation stage is empty
-        e = launch_route_small(x, w_router, bias, cfg->T, cfg->d, cfg->N, cfg->M, cfg->k_per_group, false,
-                               cfg->act_dtype, at<float>(ws, L.logits), a.logits, idx, gate,
-                               at<uint32_t>(ws, kTicketOffset), at<uint32_t>(ws, L.status), counts, offsets,
-                               pair_row, row_token, a.group_load, a.score, st);
-        if (e != cudaSuccess) return cuda_status(e);
-        mark_stage(MOGE_STAGE_PERMUTE, st);
-    } else {
-        if ((s = route_impl(cfg, MOGE_ROUTE_GROUPED, x, w_router, bias, a.logits, idx, gate, ws, st)) != MOGE_OK)
-            return s;
-        mark_stage(MOGE_STAGE_PERMUTE, st);  // the permutation also writes the imbalance outputs
-        e = launch_permute(idx, cfg->T, K, cfg->N, counts, offsets, pair_row, row_token,
-                           at<int32_t>(ws, L.chunk_counts), at<uint32_t>(ws, L.status), st, cfg->M, a.group_load,
-                           a.score);
-    }
-    // Few tokens (weights-as-M tiles): the gate/up GEMM gathers the token rows itself (TMA gather4
-    // through row_token) and the gather stage is empty.  Many tokens: 32 gather4 copies per
-    // k-block would throttle the TMA unit, so rows are first copied to x_perm and loaded as tiles.
-    const bool gather_in_gemm = gathers_in_gemm(*cfg);
-    mark_stage(MOGE_STAGE_GATHER, st);
-    if (e == cudaSuccess && !gather_in_gemm)
-        e = launch_gather_rows(x, row_token, offsets, cfg->N, P, cfg->d, cfg->act_dtype, x_perm, st);
-    if (e != cudaSuccess) return cuda_status(e);
-    mark_stage(MOGE_STAGE_GATE_UP, st);  // the FFN marks MOGE_STAGE_DOWN between its two GEMMs
-    s = gather_in_gemm ? ffn_impl(cfg, x, row_token, offsets, w_gate, w_up, w_down, y_perm, ws, st)
-                       : ffn_impl(cfg, x_perm, nullptr, offsets, w_gate, w_up, w_down, y_perm, ws, st);
-    if (s != MOGE_OK) return s;
-    mark_stage(MOGE_STAGE_COMBINE, st);
-    e = launch_combine(y_perm, pair_row, gate, cfg->T, K, cfg->d, cfg->act_dtype, y, st);
-    mark_stage(MOGE_STAGE_IMBALANCE, st);  // empty: computed with the permutation
-    mark_stage(MOGE_NUM_STAGES, st);
-    return cuda_status(e);
+size_t moge_workspace_bytes_shared(const moge_config_t *cfg, int64_t n_shared) {
+    if (n_shared < 0 || n_shared > kMaxShared || check_routing(cfg) != MOGE_OK) return 0;
+    moge_config_t c = *cfg;
+    if (c.d < 0 || c.I < 0) return 0;
+    if (c.act_dtype != MOGE_BF16) c.act_dtype = MOGE_F32;
+    return ws_layout(c, n_shared).total;
+}
+
+moge_status_t moge_layer_forward_shared(const moge_config_t *cfg, int64_t n_shared, const void *x,
+                                        const void *w_router, const float *bias, const void *w_gate,
+                                        const void *w_up, const void *w_down, void *y, const moge_aux_t *aux,
+                                        void *ws, size_t ws_bytes, moge_stream_t stream) {
+    return layer_impl(cfg, n_shared, x, w_router, bias, w_gate, w_up, w_down, y, aux, ws, ws_bytes, stream);
 }
 
 moge_status_t moge_imbalance_study(const moge_config_t *cfg, int64_t batches, uint64_t seed, const float *bias,

@@ -1,5 +1,6 @@
 // Weighted combine: y[t,:] = sum_{k=0..K-1} gate[t,k] * y_perm[pair_row[t,k],:], summed in
-// slot order with fp32 accumulation and rounded once to the activation dtype.
+// slot order with fp32 accumulation and rounded once to the activation dtype; with S shared
+// experts their rows y_perm[shared_base + s*T + t,:] follow with weight 1, in order s = 0..S-1.
 // Grid (token, column block): each thread owns one 16-byte column vector of one token and
 // issues the loads of 8 slots before their FMAs, so the reads of y_perm stay in flight
 // together instead of one round trip per slot.
@@ -13,7 +14,7 @@ constexpr int kSlotBatch = 8;
 template <typename T, int V>  // V elements per 16-byte vector
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_row, const float *__restrict__ gate,
-               int K, int64_t d, T *__restrict__ y) {
+               int K, int64_t d, T *__restrict__ y, int S, int64_t shared_base, int64_t Tn) {
     const int64_t t = blockIdx.x;
     const int64_t v = (int64_t)blockIdx.y * kCombineThreads + threadIdx.x;
     const int64_t nvec = d / V;
@@ -41,6 +42,21 @@ combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_ro
             for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], to_f32(e[i]), acc[i]);
         }
     }
+    for (int s0 = 0; s0 < S; s0 += kSlotBatch) {
+        int4 raw[kSlotBatch];
+#pragma unroll
+        for (int j = 0; j < kSlotBatch; ++j) {
+            const int64_t row = shared_base + (int64_t)(s0 + j) * Tn + t;
+            raw[j] = s0 + j < S ? __ldg(reinterpret_cast<const int4 *>(y_perm + row * d) + v) : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < kSlotBatch; ++j) {
+            if (s0 + j >= S) break;
+            const T *e = reinterpret_cast<const T *>(&raw[j]);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] += to_f32(e[i]);
+        }
+    }
     int4 out;
     T *o = reinterpret_cast<T *>(&out);
 #pragma unroll
@@ -49,16 +65,16 @@ combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_ro
 }
 
 cudaError_t launch_combine(const void *y_perm, const int32_t *pair_row, const float *gate, int64_t T,
-                           int64_t K, int64_t d, int dtype, void *y, cudaStream_t s) {
+                           int64_t K, int64_t d, int dtype, void *y, cudaStream_t s, int64_t S, int64_t shared_base) {
     if (T == 0) return cudaSuccess;
     const int V = dtype == MOGE_BF16 ? 8 : 4;
     dim3 grid((unsigned)T, (unsigned)cdiv(d / V, kCombineThreads));
     if (dtype == MOGE_BF16)
         combine_kernel<__nv_bfloat16, 8><<<grid, kCombineThreads, 0, s>>>(
-            (const __nv_bfloat16 *)y_perm, pair_row, gate, (int)K, d, (__nv_bfloat16 *)y);
+            (const __nv_bfloat16 *)y_perm, pair_row, gate, (int)K, d, (__nv_bfloat16 *)y, (int)S, shared_base, T);
     else
         combine_kernel<float, 4><<<grid, kCombineThreads, 0, s>>>((const float *)y_perm, pair_row, gate, (int)K,
-                                                                   d, (float *)y);
+                                                                   d, (float *)y, (int)S, shared_base, T);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -82,9 +82,12 @@ static_assert(kSmallRouteMaxT <= kPermuteChunk, "the small router permutes its t
 // (TMA gather4); every other layer reads a permuted copy x_perm.
 inline bool gathers_in_gemm(const moge_config_t &c) { return c.act_dtype == MOGE_BF16 && c.T <= 64; }
 
-inline WsLayout ws_layout(const moge_config_t &c) {
+// S shared experts (every token visits each of them; rows P + s*T + t) extend the expert index
+// space to N + S and the rows to P + S*T.
+inline WsLayout ws_layout(const moge_config_t &c, int64_t S = 0) {
     const int64_t K = c.M * c.k_per_group;
     const int64_t P = c.T * K;
+    const int64_t rows = P + S * c.T;
     const size_t es = (c.act_dtype == MOGE_BF16) ? 2 : 4;
     const int64_t chunks = cdiv(c.T > 0 ? c.T : 1, kPermuteChunk);
     WsLayout L{};
@@ -95,18 +98,18 @@ inline WsLayout ws_layout(const moge_config_t &c) {
     L.idx = take((size_t)P * 4);
     L.gate = take((size_t)P * 4);
     L.counts = take((size_t)c.N * 4);
-    L.offsets = take((size_t)(c.N + 1) * 4);
+    L.offsets = take((size_t)(c.N + S + 1) * 4);
     L.pair_row = take((size_t)P * 4);
-    L.row_token = take((size_t)P * 4);
+    L.row_token = take((size_t)rows * 4);
     L.chunk_counts = take((size_t)chunks * c.N * 4);
     {
         const int s = router_kslices(c.T, c.d, c.N);
         L.router_partials = take(s > 1 ? (size_t)cdiv(c.T, kRouterTileRows) * s * kRouterTileRows * c.N * 4 : 0);
     }
     // layers whose gate/up GEMM gathers token rows itself store no permuted copy of x
-    L.x_perm = take(gathers_in_gemm(c) ? 0 : (size_t)P * c.d * es);
-    L.h = take((size_t)P * c.I * es);
-    L.y_perm = take((size_t)P * c.d * es);
+    L.x_perm = take(gathers_in_gemm(c) ? 0 : (size_t)rows * c.d * es);
+    L.h = take((size_t)rows * c.I * es);
+    L.y_perm = take((size_t)rows * c.d * es);
     L.total = off;
     return L;
 }
@@ -147,8 +150,14 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const in
                                int64_t N, int64_t P, int64_t d, int dtype, void *x_perm, cudaStream_t s);
 cudaError_t launch_imbalance(const int32_t *counts, int64_t T, int64_t N, int64_t M, int32_t *group_load,
                              float *score, cudaStream_t s);
+// y[t] = sum_k gate[t,k] * y_perm[pair_row[t,k]] + sum_{s<S} y_perm[shared_base + s*T + t]
 cudaError_t launch_combine(const void *y_perm, const int32_t *pair_row, const float *gate, int64_t T,
-                           int64_t K, int64_t d, int dtype, void *y, cudaStream_t s);
+                           int64_t K, int64_t d, int dtype, void *y, cudaStream_t s, int64_t S = 0,
+                           int64_t shared_base = 0);
+// Rows of S shared experts after the P routed rows: offsets[N+1+s] = P + (s+1)*T and
+// row_token[P + s*T + t] = t (offsets[N] = P is the permutation's).
+cudaError_t launch_shared_rows(int64_t T, int64_t N, int64_t S, int64_t P, int32_t *offsets, int32_t *row_token,
+                               cudaStream_t s);
 cudaError_t launch_ffn_simt(const void *x_perm, const int32_t *offsets, int64_t N, int64_t P, int64_t d,
                             int64_t I, int dtype, const void *w_gate, const void *w_up, const void *w_down,
                             void *h, void *y_perm, cudaStream_t s);

@@ -186,6 +186,28 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const in
 }
 
 // ---------------------------------------------------------------------------------------------
+// Shared experts: every token visits each of the S shared experts, so their rows are fixed:
+// expert N + s owns rows [P + s*T, P + (s+1)*T), row P + s*T + t holding token t.
+// ---------------------------------------------------------------------------------------------
+__global__ void shared_rows_kernel(int64_t T, int64_t N, int64_t S, int64_t P, int32_t *__restrict__ offsets,
+                                   int32_t *__restrict__ row_token) {
+    const int64_t n = S * T;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        row_token[P + i] = (int32_t)(i % T);
+    if (blockIdx.x == 0)
+        for (int64_t s = threadIdx.x; s < S; s += blockDim.x) offsets[N + 1 + s] = (int32_t)(P + (s + 1) * T);
+}
+
+cudaError_t launch_shared_rows(int64_t T, int64_t N, int64_t S, int64_t P, int32_t *offsets, int32_t *row_token,
+                               cudaStream_t s) {
+    if (S == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(cdiv(S * T, 256), 1184));
+    shared_rows_kernel<<<blocks, 256, 0, s>>>(T, N, S, P, offsets, row_token);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
 // Imbalance score: group loads, then (max - min) / T.  One block.
 // ---------------------------------------------------------------------------------------------
 __global__ void imbalance_kernel(const int32_t *__restrict__ counts, int64_t T, int N, int M,

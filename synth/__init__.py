@@ -125,11 +125,13 @@ def route_logits(seed: int, T: int, N: int) -> np.ndarray:
     return (noise + router_bias(seed, N)[None, :]).astype(np.float32)
 
 
-def layer_inputs(w: "Workload", seed: int = DEFAULT_SEED, with_experts: bool = True) -> dict:
+def layer_inputs(w: "Workload", seed: int = DEFAULT_SEED, with_experts: bool = True, n_shared: int = 0) -> dict:
     """All inputs of one MoGE layer workload as host arrays.
 
     Activations and weights are fp32 for an fp32 workload, else raw bf16 bits.
-    The router bias is always fp32 (zero when the workload has no skew).
+    The router bias is always fp32 (zero when the workload has no skew).  With
+    n_shared > 0 the expert weights hold N + n_shared experts: the routed ones
+    (the same values as without shared experts) followed by the shared ones.
     """
     dt = w.dtype
     T, d, N, I = w.T, w.d, w.N, w.I
@@ -139,9 +141,10 @@ def layer_inputs(w: "Workload", seed: int = DEFAULT_SEED, with_experts: bool = T
         "bias": router_bias(seed, N) if w.skew else np.zeros(N, dtype=np.float32),
     }
     if with_experts:
-        out["w_gate"] = normal(seed, TID_WGATE, (N, I, d), d ** -0.5, dt)
-        out["w_up"] = normal(seed, TID_WUP, (N, I, d), d ** -0.5, dt)
-        out["w_down"] = normal(seed, TID_WDOWN, (N, d, I), I ** -0.5, dt)
+        E = N + n_shared
+        out["w_gate"] = normal(seed, TID_WGATE, (E, I, d), d ** -0.5, dt)
+        out["w_up"] = normal(seed, TID_WUP, (E, I, d), d ** -0.5, dt)
+        out["w_down"] = normal(seed, TID_WDOWN, (E, d, I), I ** -0.5, dt)
     return out
 
 

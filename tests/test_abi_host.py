@@ -131,3 +131,20 @@ def test_imbalance_study_rejects_bad_arguments():
     bad = cfg(T=64, N=15, M=4, kpg=1)
     assert f(ctypes.byref(bad), 4, 1, None, FAKE, FAKE, None, None, None) == INVALID
     assert f(None, 4, 1, None, FAKE, FAKE, None, None, None) == INVALID
+
+
+def test_shared_layer_workspace_and_argument_checks():
+    c = cfg(T=64, N=16, M=4, kpg=1)
+    base = moge.moge_workspace_bytes(c)
+    assert moge.moge_workspace_bytes_shared(c, 0) == base
+    assert moge.moge_workspace_bytes_shared(c, 4) > base
+    assert moge.moge_workspace_bytes_shared(c, -1) == 0 and moge.moge_workspace_bytes_shared(c, 65) == 0
+    lib = binding.load()
+    f = lib.moge_layer_forward_shared
+    big = 1 << 40
+    assert f(ctypes.byref(c), -1, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, big, None) == INVALID
+    assert f(ctypes.byref(c), 65, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, big, None) == INVALID
+    wide = cfg(T=64, N=1024, M=4, kpg=1)
+    assert f(ctypes.byref(wide), 4, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, big, None) == UNSUPPORTED
+    small_ws = moge.moge_workspace_bytes_shared(c, 4) - 256
+    assert f(ctypes.byref(c), 4, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, small_ws, None) == WORKSPACE
