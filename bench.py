@@ -470,6 +470,26 @@ def run_ours(args):
                             "tflops": round(6.0 * rows * w.d * w.I / (sms / 1e3) / 1e12, 2)}
             del L
 
+    # Pangu Pro MoE's own dimensions: hidden 5120, top-1 per group (K = 8), 4 shared experts
+    pangu = None
+    if args.pangu_steps > 0:
+        pangu = {"n_shared": SHARED_EXPERTS}
+        wpp, wpd = WORKLOADS["pangu_k1_t8192"], WORKLOADS["pangu_k1_t32"]
+        p_inp = upload(synth.layer_inputs(wpp, seed=DEFAULT_SEED, n_shared=SHARED_EXPERTS), device)
+        for name, w, n in (("prefill", wpp, args.pangu_steps), ("decode", wpd, 3 * args.pangu_steps)):
+            L = Layer(w, p_inp, device, n_shared=SHARED_EXPERTS)
+            pms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist)
+            rows = w.P + SHARED_EXPERTS * w.T
+            touched = int((L.aux["counts"].cpu().numpy() > 0).sum()) + SHARED_EXPERTS
+            pangu[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "d": w.d, "I": w.I, "K": w.K,
+                           "value": round(w.T * ws_n / (pms / 1e3), 1), "unit": "tokens/s",
+                           "ms_per_step": round(pms, 4), "steps": n,
+                           "tflops": round(6.0 * rows * w.d * w.I / (pms / 1e3) / 1e12, 2),
+                           "weight_gbs": round(touched * 3 * w.d * w.I * 2 / (pms / 1e3) / 1e9, 1),
+                           "touched_experts": touched}
+            del L
+        del p_inp
+
     # Monte-Carlo imbalance study on the routing workload's shape (MoGE vs global top-K)
     study = None
     if args.study_batches > 0:
@@ -510,6 +530,7 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "decode": decode,
         "shared_experts": shared,
+        "pangu_dims_k1": pangu,
         "imbalance_study": study,
     }
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
@@ -613,6 +634,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
     ap.add_argument("--shared-steps", type=int, default=50, help="steps of the shared-expert layers (0: skip)")
     ap.add_argument("--study-batches", type=int, default=1000, help="Monte-Carlo study batches (0: skip)")
+    ap.add_argument("--pangu-steps", type=int, default=30, help="steps at Pangu Pro dims, K'=1 (0: skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle FFN work")

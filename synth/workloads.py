@@ -4,7 +4,12 @@ K' (experts per group) is explicit in every workload; K = M * K'.  The
 routing-only workload is also run at K' = 1.  The prefill and decode layers
 share one layer shape (d=4096, N=64 in 8 groups, K'=2, I=1408); the stress
 layer borrows the Pangu Ultra MoE dimensions (d=7680, N=256, I=2048) with
-MoGE routing imposed on them.
+MoGE routing imposed on them.  The two "pangu_k1" layers take Pangu Pro MoE's
+own dimensions (hidden 5120, 64 routed experts in 8 groups, top-1 per group,
+i.e. K = 8; 4 shared experts are added where they are measured) with an expert
+intermediate size of 1344, which the pages do not give: 48 layers x 68 experts
+x 3*5120*1344 weights is about 67 B parameters, consistent with the 72 B total
+they print once attention and embeddings are counted.
 """
 from __future__ import annotations
 
@@ -53,4 +58,8 @@ WORKLOADS = {
                               dtype="bf16", skew=True),
     "stress_n256": Workload("stress_n256", T=4096, d=7680, N=256, M=8, kpg=1, I=2048,
                             dtype="bf16", skew=True),
+    "pangu_k1_t32": Workload("pangu_k1_t32", T=32, d=5120, N=64, M=8, kpg=1, I=1344,
+                             dtype="bf16", skew=True),
+    "pangu_k1_t8192": Workload("pangu_k1_t8192", T=8192, d=5120, N=64, M=8, kpg=1, I=1344,
+                               dtype="bf16", skew=True),
 }
