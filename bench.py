@@ -52,6 +52,21 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(ms: float, dist: bool, device) -> float:
+    """The slowest rank's time (weak-scaling replicas: the job is done when every rank is)."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput of `world` independent replicas: all tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_max / 1e3)
+
+
 def peaks():
     if os.path.exists(PEAKS_PATH):
         with open(PEAKS_PATH) as f:
@@ -236,11 +251,7 @@ def timed_steps(layer, steps, warmup, dist, clock=None):
     launches = moge.moge_kernel_launch_count() - n0
     if dist:
         torch.distributed.barrier()
-    ms = start.elapsed_time(end) / steps
-    if dist:
-        t = torch.tensor([ms], device=layer.dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end) / steps, dist, layer.dev)
     gate_up_ms = statistics.fmean(e[gu].elapsed_time(e[gu + 1]) for e in evs)
     if moge.moge_query_device_status(layer.ws) != 0:
         raise RuntimeError("device status reports a timed-out wait")
@@ -312,11 +323,7 @@ def e2e_steps(layer, steps, dist):
     run(steps)
     end.record(comp)
     torch.cuda.synchronize()
-    ms = start.elapsed_time(end) / steps
-    if dist:
-        t = torch.tensor([ms], device=layer.dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end) / steps, dist, layer.dev)
     return ms, x_host[0].numel() * 2, y_host[0].numel() * 2
 
 
@@ -451,7 +458,7 @@ def run_ours(args):
         dms, dgate_up_ms, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist)
         dstages = stage_breakdown(dec, min(args.decode_steps, 100))
         dcounts = dec.aux["counts"].cpu().numpy()
-        decode = {"workload": wd.name, "value": round(wd.T * ws_n / (dms / 1e3), 1), "unit": "tokens/s",
+        decode = {"workload": wd.name, "value": round(job_tokens_per_s(wd.T, ws_n, dms), 1), "unit": "tokens/s",
                   "ms_per_step": round(dms, 4), "steps": args.decode_steps,
                   "roofline": gate_up_roofline(wd, dcounts, dgate_up_ms, pk, peak_kind),
                   "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
@@ -465,7 +472,7 @@ def run_ours(args):
             L = Layer(w, d_inp, device, n_shared=SHARED_EXPERTS)
             sms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist)
             rows = w.P + SHARED_EXPERTS * w.T
-            shared[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "value": round(w.T * ws_n / (sms / 1e3), 1),
+            shared[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "value": round(job_tokens_per_s(w.T, ws_n, sms), 1),
                             "unit": "tokens/s", "ms_per_step": round(sms, 4), "steps": n,
                             "tflops": round(6.0 * rows * w.d * w.I / (sms / 1e3) / 1e12, 2)}
             del L
@@ -482,7 +489,7 @@ def run_ours(args):
             rows = w.P + SHARED_EXPERTS * w.T
             touched = int((L.aux["counts"].cpu().numpy() > 0).sum()) + SHARED_EXPERTS
             pangu[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "d": w.d, "I": w.I, "K": w.K,
-                           "value": round(w.T * ws_n / (pms / 1e3), 1), "unit": "tokens/s",
+                           "value": round(job_tokens_per_s(w.T, ws_n, pms), 1), "unit": "tokens/s",
                            "ms_per_step": round(pms, 4), "steps": n,
                            "tflops": round(6.0 * rows * w.d * w.I / (pms / 1e3) / 1e12, 2),
                            "weight_gbs": round(touched * 3 * w.d * w.I * 2 / (pms / 1e3) / 1e9, 1),
@@ -499,14 +506,13 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e_ms, h2d, d2h = e2e_steps(prefill, max(3, args.steps // 2), dist)
-        e2e = {"value": round(wp.T * ws_n / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": round(job_tokens_per_s(wp.T, ws_n, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                "copies": "pinned host buffers; upload of step i+1 and download of step i-1 overlap step i"}
 
-    tok = wp.T * ws_n
     res = {
         "metric": METRIC,
-        "value": round(tok / (ms / 1e3), 1),
+        "value": round(job_tokens_per_s(wp.T, ws_n, ms), 1),
         "unit": "tokens/s",
         "n_gpus": ws_n,
         "steps": args.steps,
