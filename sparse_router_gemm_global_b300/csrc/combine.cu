@@ -15,6 +15,8 @@ template <typename T, int V>  // V elements per 16-byte vector
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_row, const float *__restrict__ gate,
                int K, int64_t d, T *__restrict__ y, int S, int64_t shared_base, int64_t Tn) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t t = blockIdx.x;
     const int64_t v = (int64_t)blockIdx.y * kCombineThreads + threadIdx.x;
     const int64_t nvec = d / V;
@@ -69,14 +71,14 @@ cudaError_t launch_combine(const void *y_perm, const int32_t *pair_row, const fl
     if (T == 0) return cudaSuccess;
     const int V = dtype == MOGE_BF16 ? 8 : 4;
     dim3 grid((unsigned)T, (unsigned)cdiv(d / V, kCombineThreads));
-    if (dtype == MOGE_BF16)
-        combine_kernel<__nv_bfloat16, 8><<<grid, kCombineThreads, 0, s>>>(
-            (const __nv_bfloat16 *)y_perm, pair_row, gate, (int)K, d, (__nv_bfloat16 *)y, (int)S, shared_base, T);
-    else
-        combine_kernel<float, 4><<<grid, kCombineThreads, 0, s>>>((const float *)y_perm, pair_row, gate, (int)K,
-                                                                   d, (float *)y, (int)S, shared_base, T);
+    cudaError_t err = dtype == MOGE_BF16
+        ? launch_pdl(combine_kernel<__nv_bfloat16, 8>, grid, dim3(kCombineThreads), 0, s,
+                     (const __nv_bfloat16 *)y_perm, pair_row, gate, (int)K, d, (__nv_bfloat16 *)y, (int)S,
+                     shared_base, T)
+        : launch_pdl(combine_kernel<float, 4>, grid, dim3(kCombineThreads), 0, s, (const float *)y_perm, pair_row,
+                     gate, (int)K, d, (float *)y, (int)S, shared_base, T);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moge

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moge.h"
 
 namespace moge {
@@ -12,6 +14,31 @@ namespace moge {
 // Kernel launch counter and per-thread stage events (instrumentation, api.cu).
 void count_launches(int n);
 void mark_stage(int stage, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch.  The layer's kernels are launched so that each may start (its
+// prologue: barriers, TMEM, descriptor prefetch) while the previous kernel in the stream
+// finishes; every such kernel calls pdl_wait() before it touches memory written by earlier
+// work, and pdl_trigger() right after, which lets its own successor be scheduled.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Status word bits (first 4 bytes of the workspace).
 enum : uint32_t {

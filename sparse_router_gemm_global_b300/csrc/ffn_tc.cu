@@ -176,6 +176,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         tmem_alloc(smem_u32(&tmem_base_slot), C::tmem_cols);
         tmem_relinquish();
     }
+    pdl_wait();  // the offsets (and the token rows) come from earlier kernels
+    pdl_trigger();
     build_prefix(p.offsets, p.N, C::tok_block, prefix, warp_sums);  // contains __syncthreads
     tc_fence_before();
     __syncthreads();
@@ -468,6 +470,8 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         tmem_alloc_pair(smem_u32(&tmem_base_slot), kPairTmemCols);
         tmem_relinquish_pair();
     }
+    pdl_wait();  // the offsets (and the token rows) come from earlier kernels
+    pdl_trigger();
     build_prefix(p.offsets, p.N, kPairRows, prefix, warp_sums);  // contains __syncthreads
     tc_fence_before();
     cluster_sync();  // both CTAs' barriers are initialised and their TMEM allocated
@@ -665,9 +669,9 @@ cudaError_t launch_mode(const CUtensorMap &ma, const CUtensorMap &mb0, const CUt
     if (err != cudaSuccess) return err;
     const int grid = (int)std::min<int64_t>(tile_bound, (int64_t)sm_count());
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, kThreads, C::smem_bytes, s>>>(ma, mb0, mb1, p);
+    err = launch_pdl(kern, dim3(grid), dim3(kThreads), C::smem_bytes, s, ma, mb0, mb1, p);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 template <bool GLU>
@@ -678,9 +682,9 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb0, const CUt
     if (err != cudaSuccess) return err;
     const int grid = (int)std::min<int64_t>(2 * pair_tile_bound, (int64_t)(sm_count() & ~1));  // whole pairs
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, kThreads, kPairSmem, s>>>(ma, mb0, mb1, p);
+    err = launch_pdl(kern, dim3(grid), dim3(kThreads), kPairSmem, s, ma, mb0, mb1, p);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 // Token rows of the gate/up GEMM: gathered from x [T, d] through row_token (one-row box), or

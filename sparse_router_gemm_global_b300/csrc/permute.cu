@@ -13,6 +13,8 @@ namespace moge {
 __global__ void permute_count_kernel(const int32_t *__restrict__ idx, int64_t T, int K, int N,
                                      int32_t *__restrict__ chunk_counts, uint32_t *status) {
     extern __shared__ uint32_t masks[];  // [kWarps][N]
+    pdl_wait();
+    pdl_trigger();
     build_masks(idx, (int64_t)blockIdx.x * kChunk, T, K, N, masks, status);
     __syncthreads();
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
@@ -27,6 +29,8 @@ __global__ void permute_scan_kernel(int32_t *__restrict__ chunk_counts, int chun
                                     int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int M,
                                     int64_t T, int32_t *__restrict__ group_load, float *__restrict__ score) {
     extern __shared__ int32_t tot[];  // [N] counts, then [M] group loads
+    pdl_wait();
+    pdl_trigger();
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
         int run = 0;
         for (int c = 0; c < chunks; ++c) {
@@ -57,6 +61,8 @@ __global__ void permute_scatter_kernel(const int32_t *__restrict__ idx, int64_t 
     uint32_t *masks = sm;                              // [kWarps][N]
     int32_t *warp_base = (int32_t *)(sm + kWarps * N);  // [kWarps][N]
     int32_t *base = warp_base + kWarps * N;             // [N]
+    pdl_wait();
+    pdl_trigger();
     build_masks(idx, (int64_t)blockIdx.x * kChunk, T, K, N, masks, nullptr);
     for (int e = threadIdx.x; e < N; e += blockDim.x)
         base[e] = offsets[e] + chunk_base[(int64_t)blockIdx.x * N + e];
@@ -71,11 +77,15 @@ __global__ void permute_single_kernel(const int32_t *__restrict__ idx, int64_t T
                                       uint32_t *status, int M, int32_t *__restrict__ group_load,
                                       float *__restrict__ score) {
     extern __shared__ uint32_t sm[];
+    pdl_wait();
+    pdl_trigger();
     permute_one_block(idx, T, K, N, counts, offsets, pair_row, row_token, status, M, group_load, score, sm);
 }
 
 __global__ void zero_counts_kernel(int N, int32_t *counts, int32_t *offsets, int M, int32_t *group_load,
                                    float *score) {
+    pdl_wait();
+    pdl_trigger();
     for (int e = threadIdx.x; e <= N; e += blockDim.x) {
         if (e < N) counts[e] = 0;
         offsets[e] = 0;
@@ -89,9 +99,10 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
                            int32_t *offsets, int32_t *pair_row, int32_t *row_token, int32_t *chunk_counts,
                            uint32_t *status, cudaStream_t s, int64_t M, int32_t *group_load, float *score) {
     if (T == 0) {
-        zero_counts_kernel<<<1, 256, 0, s>>>((int)N, counts, offsets, (int)M, group_load, score);
+        cudaError_t err = launch_pdl(zero_counts_kernel, dim3(1), dim3(256), 0, s, (int)N, counts, offsets, (int)M,
+                                     group_load, score);
         count_launches(1);
-        return cudaGetLastError();
+        return err;
     }
     const size_t smem_scatter = (size_t)permute_block_smem_words((int)N, (int)M) * 4;
     cudaError_t err;
@@ -99,11 +110,10 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
         err = cudaFuncSetAttribute(permute_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem_scatter);
         if (err != cudaSuccess) return err;
-        permute_single_kernel<<<1, kChunk, smem_scatter, s>>>(idx, T, (int)K, (int)N, counts, offsets,
-                                                              pair_row, row_token, status, (int)M, group_load,
-                                                              score);
+        err = launch_pdl(permute_single_kernel, dim3(1), dim3(kChunk), smem_scatter, s, idx, T, (int)K, (int)N,
+                         counts, offsets, pair_row, row_token, status, (int)M, group_load, score);
         count_launches(1);
-        return cudaGetLastError();
+        return err;
     }
     const int chunks = (int)cdiv(T, kChunk);
     const size_t smem_count = (size_t)kWarps * N * 4;
@@ -113,15 +123,18 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
     err = cudaFuncSetAttribute(permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem_scatter);
     if (err != cudaSuccess) return err;
-    permute_count_kernel<<<chunks, kChunk, smem_count, s>>>(idx, T, (int)K, (int)N, chunk_counts, status);
+    err = launch_pdl(permute_count_kernel, dim3(chunks), dim3(kChunk), smem_count, s, idx, T, (int)K, (int)N,
+                     chunk_counts, status);
     count_launches(1);
-    permute_scan_kernel<<<1, 1024, (size_t)(N + M) * 4, s>>>(chunk_counts, chunks, (int)N, counts, offsets,
-                                                             (int)M, T, group_load, score);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), (size_t)(N + M) * 4, s, chunk_counts, chunks, (int)N,
+                     counts, offsets, (int)M, T, group_load, score);
     count_launches(1);
-    permute_scatter_kernel<<<chunks, kChunk, smem_scatter, s>>>(idx, T, (int)K, (int)N, chunk_counts,
-                                                                offsets, pair_row, row_token);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(permute_scatter_kernel, dim3(chunks), dim3(kChunk), smem_scatter, s, idx, T, (int)K, (int)N,
+                     (const int32_t *)chunk_counts, (const int32_t *)offsets, pair_row, row_token);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -146,6 +159,8 @@ __global__ void gather_rows_kernel(const int4 *__restrict__ x, const int32_t *__
     constexpr int kBatch = 8;
     uint64_t keep;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+    pdl_wait();
+    pdl_trigger();
     const int64_t rows = offsets[N];
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -180,9 +195,10 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const in
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t want = cdiv(P, 8);  // 8 warps (rows in flight) per block
     const unsigned blocks = (unsigned)std::min<int64_t>(want, (int64_t)sms * 8);
-    gather_rows_kernel<<<blocks, 256, 0, s>>>((const int4 *)x, row_token, offsets, (int)N, vec, (int4 *)x_perm);
+    cudaError_t err = launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, (const int4 *)x, row_token,
+                                 offsets, (int)N, vec, (int4 *)x_perm);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -191,6 +207,8 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const in
 // ---------------------------------------------------------------------------------------------
 __global__ void shared_rows_kernel(int64_t T, int64_t N, int64_t S, int64_t P, int32_t *__restrict__ offsets,
                                    int32_t *__restrict__ row_token) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t n = S * T;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         row_token[P + i] = (int32_t)(i % T);
@@ -202,9 +220,9 @@ cudaError_t launch_shared_rows(int64_t T, int64_t N, int64_t S, int64_t P, int32
                                cudaStream_t s) {
     if (S == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(cdiv(S * T, 256), 1184));
-    shared_rows_kernel<<<blocks, 256, 0, s>>>(T, N, S, P, offsets, row_token);
+    cudaError_t err = launch_pdl(shared_rows_kernel, dim3(blocks), dim3(256), 0, s, T, N, S, P, offsets, row_token);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -213,6 +231,8 @@ cudaError_t launch_shared_rows(int64_t T, int64_t N, int64_t S, int64_t P, int32
 __global__ void imbalance_kernel(const int32_t *__restrict__ counts, int64_t T, int N, int M,
                                  int32_t *__restrict__ group_load, float *__restrict__ score) {
     extern __shared__ int64_t loads[];  // [M]
+    pdl_wait();
+    pdl_trigger();
     const int G = N / M;
     for (int g = threadIdx.x; g < M; g += blockDim.x) {
         int64_t sum = 0;
@@ -233,9 +253,10 @@ __global__ void imbalance_kernel(const int32_t *__restrict__ counts, int64_t T, 
 
 cudaError_t launch_imbalance(const int32_t *counts, int64_t T, int64_t N, int64_t M, int32_t *group_load,
                              float *score, cudaStream_t s) {
-    imbalance_kernel<<<1, 256, (size_t)M * 8, s>>>(counts, T, (int)N, (int)M, group_load, score);
+    cudaError_t err = launch_pdl(imbalance_kernel, dim3(1), dim3(256), (size_t)M * 8, s, counts, T, (int)N, (int)M,
+                                 group_load, score);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moge

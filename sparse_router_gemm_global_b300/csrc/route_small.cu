@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const Params p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * kTokTile;
     const int e0 = blockIdx.y * kExpTile;
+    pdl_wait();
+    pdl_trigger();
 
     // ---- scores of this CTA's kTokTile x kExpTile tile.  Thread i of the block owns the 16-byte
     // vectors i, i + 256, ... of the hidden dimension for every token and expert of the tile,
@@ -300,15 +302,15 @@ cudaError_t launch_route_small(const void *x, const void *w_r, const float *bias
         err = cudaFuncSetAttribute(route_small_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem);
         if (err != cudaSuccess) return err;
-        route_small_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(p);
+        err = launch_pdl(route_small_kernel<__nv_bfloat16>, grid, dim3(kThreads), smem, s, p);
     } else {
         err = cudaFuncSetAttribute(route_small_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem);
         if (err != cudaSuccess) return err;
-        route_small_kernel<float><<<grid, kThreads, smem, s>>>(p);
+        err = launch_pdl(route_small_kernel<float>, grid, dim3(kThreads), smem, s, p);
     }
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moge

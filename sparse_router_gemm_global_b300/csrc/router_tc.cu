@@ -79,6 +79,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem = tmem_slot;
     volatile int *abort_v = &abort_flag;
 
@@ -283,9 +285,9 @@ cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, 
     cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid((unsigned)cdiv(T, kBM), (unsigned)p.kslices);
-    router_tc_kernel<<<grid, kThreads, smem, s>>>(mx, mw, p);
+    err = launch_pdl(router_tc_kernel, grid, dim3(kThreads), smem, s, mx, mw, p);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moge
