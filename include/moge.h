@@ -267,6 +267,17 @@ typedef enum {
  * The array is read at each call, so it must stay valid while recording is on. */
 moge_status_t moge_set_stage_events(void *const *events, int n);
 
+/* Failure-detection self-test (no counterpart on the pages): one small kernel
+ * runs the bounded mbarrier wait used by the tensor-core kernels on barriers
+ * that nothing completes.  One wait gives up after timeout_ns (1 ns .. 1 s),
+ * raises the kernel's abort flag and records MOGE_ERR_TIMEOUT in the status
+ * word of ws (read it with moge_query_device_status, clear it with
+ * moge_reset_device_status); a second wait, with a longer limit, must leave
+ * through the abort flag.  result (device, 16-byte aligned, 3 words) receives
+ * {wait 1 succeeded, wait 2 succeeded, abort flag}: {0, 0, 1} when the
+ * machinery works.  Nothing faults or hangs; the GPU stays usable. */
+moge_status_t moge_selftest_bounded_wait(void *ws, uint64_t timeout_ns, uint32_t *result, moge_stream_t stream);
+
 /* Number of kernels this library has launched since it was loaded (all host
  * threads).  Lets a caller count the device work behind a region of calls. */
 uint64_t moge_kernel_launch_count(void);

@@ -78,10 +78,11 @@ def load():
         lib.moge_workspace_bytes_shared.argtypes = [cfgp, ctypes.c_int64]
         lib.moge_layer_forward_shared.argtypes = [cfgp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp,
                                                   ctypes.POINTER(Aux), vp, sz, vp]
+        lib.moge_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint64, vp, vp]
         lib.moge_imbalance_study.argtypes = [cfgp, ctypes.c_int64, ctypes.c_uint64, vp, vp, vp, vp, vp, vp]
         lib.moge_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         lib.moge_kernel_launch_count.restype = ctypes.c_uint64
-        for fn in ("moge_layer_forward_shared", "moge_imbalance_study", "moge_set_stage_events", "moge_reset_device_status", "moge_query_device_status", "moge_route", "moge_permute",
+        for fn in ("moge_selftest_bounded_wait", "moge_layer_forward_shared", "moge_imbalance_study", "moge_set_stage_events", "moge_reset_device_status", "moge_query_device_status", "moge_route", "moge_permute",
                    "moge_expert_ffn", "moge_combine", "moge_imbalance_score", "moge_layer_forward"):
             getattr(lib, fn).restype = i32
         _lib = lib
@@ -223,6 +224,11 @@ def moge_imbalance_study(cfg, batches, seed, bias, loads_grouped, loads_global, 
     _check("moge_imbalance_study", load().moge_imbalance_study(
         ctypes.byref(cfg), int(batches), int(seed), _ptr(bias), _ptr(loads_grouped), _ptr(loads_global),
         _ptr(is_grouped), _ptr(is_global), _stream(stream)))
+
+
+def moge_selftest_bounded_wait(ws, timeout_ns, result, stream=None) -> None:
+    _check("moge_selftest_bounded_wait", load().moge_selftest_bounded_wait(_ptr(ws), int(timeout_ns), _ptr(result),
+                                                                           _stream(stream)))
 
 
 def moge_kernel_launch_count() -> int:

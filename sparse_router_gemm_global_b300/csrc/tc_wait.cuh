@@ -13,14 +13,14 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 // flag is raised by another role, or after kWaitTimeoutNs, in which case it raises the flag
 // itself and records MOGE_ERR_TIMEOUT in the workspace status word.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         uint32_t *status) {
+                                         uint32_t *status, uint64_t timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 31) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs || n > (1u << 30)) {
+            if (globaltimer() - t0 > timeout_ns || n > (1u << 30)) {
                 *abort_flag = 1;
                 raise_status(status, kStatusTimeout);
                 return false;
