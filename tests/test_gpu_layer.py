@@ -148,3 +148,42 @@ def test_stress_n256_sampled():
     rng = np.random.default_rng(2)
     toks = np.sort(rng.choice(w.T, 24, replace=False))
     check_layer(w, inp, got, tokens=toks)
+
+
+@pytest.mark.parametrize("T", [16, 17, 32, 33, 64, 65, 256, 257])
+def test_bf16_layer_at_path_boundaries(T):
+    """Token counts on both sides of every switch: weights-as-M tile widths 16/32/64, the
+    weights-as-M -> tokens-as-M switch (64/65), the small router (64), one vs several
+    permutation chunks (256/257)."""
+    w = WORKLOADS["decode_t32"].with_(name=f"edge_{T}", T=T, d=384, I=192)
+    inp = synth.layer_inputs(w, seed=100 + T)
+    got = run_layer(w, upload_layer(inp))
+    check_layer(w, inp, got)
+
+
+def test_fp32_layer_many_tokens():
+    w = WORKLOADS["tiny_fp32"].with_(name="fp32_t300", T=300, d=128, I=64)
+    inp = synth.layer_inputs(w, seed=12)
+    got = run_layer(w, upload_layer(inp))
+    check_layer(w, inp, got)
+
+
+@pytest.mark.parametrize("T", [5, 48])
+def test_expert_ffn_standalone_few_tokens(T):
+    """moge_expert_ffn on an oracle permutation at weights-as-M sizes (rows read from x_perm)."""
+    w = WORKLOADS["decode_t32"].with_(T=T, d=256, I=192)
+    inp = synth.layer_inputs(w, seed=6 + T)
+    ref = oracle.layer_forward(inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                               inp["w_down"], w.M, w.kpg)
+    c = config(w)
+    ws = moge.alloc_workspace(c)
+    x_perm = dev(inp["x"][ref["row_token"]])
+    y_perm = torch.empty((w.P, w.d), dtype=torch.bfloat16, device=DEV)
+    d_inp = upload_layer(inp)
+    moge.moge_expert_ffn(c, x_perm, dev(ref["offsets"]), d_inp["w_gate"], d_inp["w_up"], d_inp["w_down"],
+                         y_perm, ws)
+    torch.cuda.synchronize()
+    experts = np.repeat(np.arange(w.N, dtype=np.int32), ref["counts"])
+    rows_ref = oracle.expert_ffn_pairs(ref["row_token"], experts, inp["x"], inp["w_gate"], inp["w_up"],
+                                       inp["w_down"])
+    assert max_rel_err(host(y_perm), rows_ref) <= TOL["bf16"]
