@@ -177,10 +177,10 @@ moge_status_t layer_impl(const moge_config_t *cfg, int64_t S, const void *x, con
     if (e == cudaSuccess) e = launch_shared_rows(cfg->T, cfg->N, S, P, offsets, row_token, st);
     if (e == cudaSuccess && a.offsets && S > 0)
         e = cudaMemcpyAsync(a.offsets, offsets, (size_t)(cfg->N + 1) * 4, cudaMemcpyDeviceToDevice, st);
-    // bf16: the gate/up GEMM gathers the token rows itself at T <= 64 (weights-as-M tiles, TMA
-    // gather4 through row_token) and the gather stage is empty; otherwise rows are first copied to
-    // x_perm and loaded as tiles.
-    const bool gather_in_gemm = gathers_in_gemm(*cfg);
+    // bf16 with at most 32 tokens: the gate/up GEMM gathers the token rows itself (TMA gather4
+    // through row_token) and the gather stage is empty; otherwise rows are first copied to x_perm
+    // and loaded as tiles.
+    const bool gather_in_gemm = gathers_in_gemm(*cfg, S);
     mark_stage(MOGE_STAGE_GATHER, st);
     if (e == cudaSuccess && !gather_in_gemm)
         e = launch_gather_rows(x, row_token, offsets, cfg->N + S, rows, cfg->d, cfg->act_dtype, x_perm, st);

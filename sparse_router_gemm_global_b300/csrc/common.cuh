@@ -105,9 +105,31 @@ constexpr int kSmallRouteMaxT = 64;
 constexpr size_t kSmallRouteMaxSmem = 160 * 1024;
 static_assert(kSmallRouteMaxT <= kPermuteChunk, "the small router permutes its tokens in one block");
 
-// bf16 layers with T <= 64 use weights-as-M tiles whose producer gathers token rows from x
-// (TMA gather4); every other layer reads a permuted copy x_perm.
-inline bool gathers_in_gemm(const moge_config_t &c) { return c.act_dtype == MOGE_BF16 && c.T <= 64; }
+// Tile plan of the bf16 grouped GEMM for `rows` (token, expert) rows over `experts` experts of a
+// batch of T tokens.  Weights-as-M tiles stream each expert's weights at full MMA height with
+// the expert's token rows as the MMA's N (16/32/64 per tile, several tiles for a larger
+// expert); they suit batches whose experts hold few rows, where 256-row tokens-as-M tiles would
+// be mostly padding.  With at most 32 tokens the GEMM gathers the token rows from x itself
+// (TMA gather4, at most 8 copies per k-block); otherwise the rows are first copied to x_perm.
+enum FfnTiles { kTilesSwap16 = 16, kTilesSwap32 = 32, kTilesSwap64 = 64, kTilesPair = 256 };
+constexpr int64_t kSwapMaxMeanRows = 96;  // weights-as-M tiles while rows / experts <= this
+struct FfnPlan {
+    int tiles;
+    bool gather_in_gemm;
+};
+inline FfnPlan ffn_plan(int64_t T, int64_t rows, int64_t experts) {
+    if (T <= 16) return {kTilesSwap16, true};
+    if (T <= 32) return {kTilesSwap32, true};
+    if (rows <= kSwapMaxMeanRows * experts) return {kTilesSwap64, false};
+    return {kTilesPair, false};
+}
+
+// Whether the layer's gate/up GEMM reads the token rows from x itself (no x_perm); fp32 layers
+// always read x_perm.
+inline bool gathers_in_gemm(const moge_config_t &c, int64_t S = 0) {
+    const int64_t rows = c.T * c.M * c.k_per_group + S * c.T;
+    return c.act_dtype == MOGE_BF16 && ffn_plan(c.T, rows, c.N + S).gather_in_gemm;
+}
 
 // S shared experts (every token visits each of them; rows P + s*T + t) extend the expert index
 // space to N + S and the rows to P + S*T.
@@ -134,7 +156,7 @@ inline WsLayout ws_layout(const moge_config_t &c, int64_t S = 0) {
         L.router_partials = take(s > 1 ? (size_t)cdiv(c.T, kRouterTileRows) * s * kRouterTileRows * c.N * 4 : 0);
     }
     // layers whose gate/up GEMM gathers token rows itself store no permuted copy of x
-    L.x_perm = take(gathers_in_gemm(c) ? 0 : (size_t)rows * c.d * es);
+    L.x_perm = take(gathers_in_gemm(c, S) ? 0 : (size_t)rows * c.d * es);
     L.h = take((size_t)rows * c.I * es);
     L.y_perm = take((size_t)rows * c.d * es);
     L.total = off;

@@ -737,14 +737,19 @@ cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32
     using namespace tc;
     if (P == 0) return cudaSuccess;
     if (N > kMaxExperts) return cudaErrorInvalidValue;
-    // A token selects an expert at most once, so no expert has more than T rows: with T <= 64
-    // every expert fits one weights-as-M tile column.
-    if (T <= 16)
-        return launch_swap<16>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
-    if (T <= 32)
-        return launch_swap<32>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
-    if (T <= 64)
-        return launch_swap<64>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status, s);
+    switch (ffn_plan(T, P, N).tiles) {
+        case kTilesSwap16:
+            return launch_swap<16>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status,
+                                   s);
+        case kTilesSwap32:
+            return launch_swap<32>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status,
+                                   s);
+        case kTilesSwap64:
+            return launch_swap<64>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status,
+                                   s);
+        default:
+            break;
+    }
     // many tokens: tokens-as-M tiles of 256 rows on CTA pairs, rows read from x_perm
     if (row_token) return cudaErrorInvalidValue;
     CUtensorMap mx, mh, mg, mu, mdn;

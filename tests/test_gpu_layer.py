@@ -150,11 +150,12 @@ def test_stress_n256_sampled():
     check_layer(w, inp, got, tokens=toks)
 
 
-@pytest.mark.parametrize("T", [16, 17, 32, 33, 64, 65, 256, 257])
+@pytest.mark.parametrize("T", [16, 17, 32, 33, 64, 65, 128, 256, 257, 384, 385])
 def test_bf16_layer_at_path_boundaries(T):
-    """Token counts on both sides of every switch: weights-as-M tile widths 16/32/64, the
-    weights-as-M -> tokens-as-M switch (64/65), the small router (64), one vs several
-    permutation chunks (256/257)."""
+    """Token counts on both sides of every switch: weights-as-M tile widths 16/32/64 and the
+    in-GEMM row gather (T <= 32), the small router (64/65), several 64-token blocks per expert
+    (128, 256), one vs several permutation chunks (256/257), weights-as-M -> tokens-as-M tiles
+    (384/385: 96 rows per expert on average with K=16 of N=64)."""
     w = WORKLOADS["decode_t32"].with_(name=f"edge_{T}", T=T, d=384, I=192)
     inp = synth.layer_inputs(w, seed=100 + T)
     got = run_layer(w, upload_layer(inp))
