@@ -43,6 +43,29 @@ constexpr int kSmemBudget = 220 * 1024;
 
 enum Mode { NORMAL_GLU = 0, NORMAL_PLAIN = 1, SWAP_GLU = 2, SWAP_PLAIN = 3 };
 
+constexpr int kPairRows = 256;  // token rows of a CTA-pair tile
+
+// Which row blocks of an expert with c rows a launch covers.
+//   kBlocksAll:       ceil(c / tok_block) blocks of tok_block rows.
+//   kBlocksPairMain:  the 256-row pair blocks, except a last block of at most 128 rows.
+//   kBlocksSmallRest: that last block (rows 256*floor(c/256) ..), as one 128-row tile.
+// PairMain + SmallRest cover every row once and keep the MMAs of a short last block from running
+// at 256 rows.
+enum BlockRule { kBlocksAll = 0, kBlocksPairMain = 1, kBlocksSmallRest = 2 };
+
+__device__ __forceinline__ int expert_blocks(int c, int tok_block, int rule) {
+    const int rest = c % kPairRows;
+    if (rule == kBlocksPairMain) return c / kPairRows + (rest > kBM ? 1 : 0);
+    if (rule == kBlocksSmallRest) return (rest > 0 && rest <= kBM) ? 1 : 0;
+    return (c + tok_block - 1) / tok_block;
+}
+
+// First row (relative to the expert's offset) and row count of block tb of an expert with c rows.
+__device__ __forceinline__ void block_rows(int c, int tb, int tok_block, int rule, int &first, int &n) {
+    first = rule == kBlocksSmallRest ? (c / kPairRows) * kPairRows : tb * tok_block;
+    n = min(tok_block, c - first);
+}
+
 template <int MODE, int BNT>
 struct Cfg {
     static constexpr bool swap = (MODE == SWAP_GLU || MODE == SWAP_PLAIN);
@@ -73,10 +96,11 @@ struct Params {
     __nv_bfloat16 *out;      // [P, out_dim]
     uint32_t *status;        // workspace status word
     const int32_t *row_token;  // [P] token of each permuted row (gathering launches only)
+    int rule;                  // BlockRule of the tile list
 };
 
-// prefix[e] = sum over e' < e of ceil(count_e' / tok_block); all 256 threads, N <= 1024.
-__device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int tok_block, int32_t *prefix,
+// prefix[e] = sum over e' < e of the row blocks of expert e' (BlockRule); all 256 threads, N <= 1024.
+__device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int tok_block, int rule, int32_t *prefix,
                              int32_t *warp_sums) {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     int v[4];
@@ -85,7 +109,7 @@ __device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int tok
     for (int i = 0; i < 4; ++i) {
         const int e = t * 4 + i;
         int b = 0;
-        if (e < N) b = (offsets[e + 1] - offsets[e] + tok_block - 1) / tok_block;
+        if (e < N) b = expert_blocks(offsets[e + 1] - offsets[e], tok_block, rule);
         local += b;
         v[i] = local;
     }
@@ -178,7 +202,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     }
     pdl_wait();  // the offsets (and the token rows) come from earlier kernels
     pdl_trigger();
-    build_prefix(p.offsets, p.N, C::tok_block, prefix, warp_sums);  // contains __syncthreads
+    build_prefix(p.offsets, p.N, C::tok_block, p.rule, prefix, warp_sums);  // contains __syncthreads
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -202,7 +226,9 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
             int e, tb, fb;
             tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
-            const int tok0 = p.offsets[e] + tb * C::tok_block;
+            int first, nrows;
+            block_rows(p.offsets[e + 1] - p.offsets[e], tb, C::tok_block, p.rule, first, nrows);
+            const int tok0 = p.offsets[e] + first;
             const int f0 = fb * C::feat_block;
             int r4[4] = {0, 0, 0, 0};
             if (gather_lane) {
@@ -307,9 +333,9 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
             tc_fence_after();
             int e, tb, fb;
             tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
-            const int cnt = p.offsets[e + 1] - p.offsets[e];
-            const int tok0 = p.offsets[e] + tb * C::tok_block;
-            const int ntok = min(C::tok_block, cnt - tb * C::tok_block);  // valid token rows of this tile
+            int first, ntok;  // ntok: valid token rows of this tile
+            block_rows(p.offsets[e + 1] - p.offsets[e], tb, C::tok_block, p.rule, first, ntok);
+            const int tok0 = p.offsets[e] + first;
             const int f0 = fb * C::feat_block;
             const uint32_t t_acc = tmem_base + acc * C::acc_cols + lane_addr;
             if constexpr (!C::swap) {
@@ -422,7 +448,6 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 // accumulator-full barriers, and both CTAs' epilogue warps arrive on its accumulator-empty
 // barrier.  Each CTA's TMEM holds its own 128 rows x 256 fp32 columns (double buffered).
 // ---------------------------------------------------------------------------------------------
-constexpr int kPairRows = 256;                   // token rows per pair tile
 constexpr int kPairStageBytes = 2 * kBM * 128;   // per CTA: 128 token rows + 128 weight rows
 constexpr int kPairStages = 6;
 constexpr size_t kPairSmem = (size_t)kPairStages * kPairStageBytes + 1024;
@@ -472,7 +497,7 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     }
     pdl_wait();  // the offsets (and the token rows) come from earlier kernels
     pdl_trigger();
-    build_prefix(p.offsets, p.N, kPairRows, prefix, warp_sums);  // contains __syncthreads
+    build_prefix(p.offsets, p.N, kPairRows, p.rule, prefix, warp_sums);  // contains __syncthreads
     tc_fence_before();
     cluster_sync();  // both CTAs' barriers are initialised and their TMEM allocated
     tc_fence_after();
@@ -704,13 +729,13 @@ cudaError_t launch_swap(const void *act, const int32_t *row_token, const int32_t
         !make_map_3d(&mdn, wd, N, d, I, kBM))
         return cudaErrorInvalidValue;
     const int64_t tok_blocks = cdiv(P, BNT) + N;
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token};
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token, kBlocksAll};
     cudaError_t err = row_token
         ? launch_mode<SWAP_GLU, BNT, true>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s)
         : launch_mode<SWAP_GLU, BNT, false>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s);
     if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
-    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr};
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksAll};
     return launch_mode<SWAP_PLAIN, BNT, false>(mh, mdn, mdn, p2, tok_blocks * cdiv(d, 128), s);
 }
 
@@ -757,13 +782,24 @@ cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32
         !make_map_3d(&mg, w_gate, N, I, d, kBM) || !make_map_3d(&mu, w_up, N, I, d, kBM) ||
         !make_map_3d(&mdn, w_down, N, d, I, kBM))
         return cudaErrorInvalidValue;
+    // 256-row pair tiles for every full block and every last block of more than 128 rows, then
+    // single-CTA 128-row tiles for the last blocks of at most 128 rows (no MMA on 128 padding rows)
     const int64_t pair_blocks = cdiv(P, kPairRows) + N;  // bound of sum_e ceil(count_e / 256)
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, nullptr};
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, nullptr, kBlocksPairMain};
     cudaError_t err = launch_pair<true>(mx, mg, mu, p1, pair_blocks * cdiv(I, 128), s);
     if (err != cudaSuccess) return err;
+    p1.rule = kBlocksSmallRest;
+    err = launch_mode<NORMAL_GLU, 0, false>(mx, mg, mu, p1, N * cdiv(I, 128), s);
+    if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
-    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr};
-    return launch_pair<false>(mh, mdn, mdn, p2, pair_blocks * cdiv(d, 256), s);
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksPairMain};
+    err = launch_pair<false>(mh, mdn, mdn, p2, pair_blocks * cdiv(d, 256), s);
+    if (err != cudaSuccess) return err;
+    // the single-CTA down tiles load all 256 W_down rows of their feature block in one box
+    CUtensorMap mdn256;
+    if (!make_map_3d(&mdn256, w_down, N, d, I, 2 * kBM)) return cudaErrorInvalidValue;
+    p2.rule = kBlocksSmallRest;
+    return launch_mode<NORMAL_PLAIN, 0, false>(mh, mdn256, mdn256, p2, N * cdiv(d, 256), s);
 }
 
 }  // namespace moge
