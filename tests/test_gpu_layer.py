@@ -188,3 +188,22 @@ def test_expert_ffn_standalone_few_tokens(T):
     rows_ref = oracle.expert_ffn_pairs(ref["row_token"], experts, inp["x"], inp["w_gate"], inp["w_up"],
                                        inp["w_down"])
     assert max_rel_err(host(y_perm), rows_ref) <= TOL["bf16"]
+
+
+def test_layer_with_1024_experts():
+    """The largest expert count the library takes (N=1024; scores on CUDA cores for N > 256)."""
+    w = WORKLOADS["decode_t32"].with_(name="n1024", T=300, d=256, N=1024, M=8, kpg=1, I=128)
+    inp = synth.layer_inputs(w, seed=31)
+    got = run_layer(w, upload_layer(inp))
+    check_layer(w, inp, got)
+
+
+@pytest.mark.slow
+def test_layer_with_half_a_million_rows():
+    """T=32768 tokens x K=16: 524288 (token, expert) rows, ~2000 CTA-pair tiles per GEMM;
+    every token's routing checked, 40 sampled output rows."""
+    w = WORKLOADS["prefill_t8192"].with_(name="rows512k", T=32768, d=256, I=128)
+    inp = synth.layer_inputs(w, seed=32)
+    got = run_layer(w, upload_layer(inp))
+    toks = np.sort(np.random.default_rng(4).choice(w.T, 40, replace=False))
+    check_layer(w, inp, got, tokens=toks)
