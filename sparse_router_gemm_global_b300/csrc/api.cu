@@ -85,8 +85,7 @@ moge_status_t route_impl(const moge_config_t *c, moge_route_mode_t mode, const v
                                               nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, st));
     if (x && c->act_dtype == MOGE_BF16 && c->N <= 256)  // scores, softmax and selection in one launch
         return cuda_status(launch_router_tc(x, w_router, bias, c->T, c->d, c->N, c->M, c->k_per_group, global,
-                                            logits, idx, gate, at<float>(ws, L.router_partials),
-                                            at<uint32_t>(ws, kTicketOffset), at<uint32_t>(ws, L.status), st));
+                                            logits, idx, gate, at<uint32_t>(ws, L.status), st));
     if (x) {
         float *dst = logits ? logits : at<float>(ws, L.logits);
         cudaError_t e = launch_router_logits_simt(x, w_router, bias, c->T, c->d, c->N, c->act_dtype, dst, st);

@@ -72,30 +72,28 @@ __device__ __forceinline__ float swiglu_precise(float a, float u) { return a / (
 // Workspace layout (every region 256-byte aligned).  Computed identically on every call.
 // ---------------------------------------------------------------------------------------------
 struct WsLayout {
-    size_t status, logits, idx, gate, counts, offsets, pair_row, row_token, chunk_counts, router_partials,
-        x_perm, h, y_perm, total;
+    size_t status, logits, idx, gate, counts, offsets, pair_row, row_token, chunk_counts, x_perm, h, y_perm, total;
 };
 
 constexpr int kPermuteChunk = 256;   // tokens per permutation block
 
 // The first kStatusPageBytes of the workspace must be zero before first use: the status word
-// sits at byte 0 and self-resetting per-tile counters of the router at kTicketOffset.
+// sits at byte 0 and the small-batch router's self-resetting counter at kTicketOffset.
 constexpr int kStatusPageBytes = 4096;
 constexpr int kTicketOffset = 256;
-constexpr int kMaxTicketTiles = (kStatusPageBytes - kTicketOffset) / 4;
 constexpr int kRouterTileRows = 128;
 constexpr int kDesignSMs = 148;  // B300 SM count: sizes the router's split of the reduction
 
 // Number of slices the tensor-core router splits its reduction over d into, so that small
-// batches still spread over more SMs (1 = no split).  At most 4 slices (each at least 16
-// k-blocks of 64): the slices are added in order by the tile's last CTA, whose latency grows
-// with their number.  Deterministic in (T, d, N).
+// batches still spread over more SMs (1 = no split).  The slices of a tile form one thread-block
+// cluster and are added in order through distributed shared memory: at most 8 (the portable
+// cluster size), each at least 8 k-blocks of 64.  Deterministic in (T, d, N).
 inline int router_kslices(int64_t T, int64_t d, int64_t N) {
     const int64_t mtiles = cdiv(T, kRouterTileRows), kblocks = cdiv(d, 64);
-    if (T <= 0 || mtiles > kMaxTicketTiles || N % 4 != 0) return 1;
+    if (T <= 0) return 1;
     int64_t s = kDesignSMs / mtiles;
-    if (s > kblocks / 16) s = kblocks / 16;
-    if (s > 4) s = 4;
+    if (s > kblocks / 8) s = kblocks / 8;
+    if (s > 8) s = 8;
     return s < 1 ? 1 : (int)s;
 }
 
@@ -151,10 +149,6 @@ inline WsLayout ws_layout(const moge_config_t &c, int64_t S = 0) {
     L.pair_row = take((size_t)P * 4);
     L.row_token = take((size_t)rows * 4);
     L.chunk_counts = take((size_t)chunks * c.N * 4);
-    {
-        const int s = router_kslices(c.T, c.d, c.N);
-        L.router_partials = take(s > 1 ? (size_t)cdiv(c.T, kRouterTileRows) * s * kRouterTileRows * c.N * 4 : 0);
-    }
     // layers whose gate/up GEMM gathers token rows itself store no permuted copy of x
     L.x_perm = take(gathers_in_gemm(c, S) ? 0 : (size_t)rows * c.d * es);
     L.h = take((size_t)rows * c.I * es);
@@ -174,7 +168,7 @@ void *tensor_map_encoder();
 // Fused tensor-core router (bf16, N <= 256): scores, softmax and selection in one launch.
 cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, int64_t T, int64_t d, int64_t N,
                              int64_t M, int64_t kpg, bool global, float *logits_out, int32_t *idx, float *gate,
-                             float *partials, uint32_t *tickets, uint32_t *status, cudaStream_t s);
+                             uint32_t *status, cudaStream_t s);
 // Small-batch router (any dtype): scores, softmax, selection and, when counts != nullptr, the
 // permutation of all T tokens (+ group loads and imbalance score) in one launch.
 bool route_small_fits(int64_t T, int64_t N, int64_t K, int64_t M, bool permute);

@@ -2,53 +2,53 @@
 // (Pangu Pro MoE explainer, section 1 "innovative architecture"), and the
 // conventional top-K over all experts it is compared with.
 //
-// One thread routes one token from a shared-memory copy of its N scores
-// (row stride N+1 keeps the per-thread reads bank-conflict free).  The
-// selection compares fp32 scores with equal scores going to the lower expert
-// index, so it is independent of how exp() rounds; the gates are
-// exp(l - max) / sum_e exp(l_e - max) with a compensated fp32 sum.
+// A block stages 64 tokens' N scores in shared memory (row stride N+1) and
+// routes them with route_rows_block: the selection compares fp32 scores with
+// equal scores going to the lower expert index, so it is independent of how
+// exp() rounds; the gates are exp(l - max) / sum_e exp(l_e - max).
 #include "common.cuh"
 #include "route_token.cuh"
 
 namespace moge {
 
-__global__ void route_select_kernel(const float *__restrict__ logits, int T, int N, int groups, int G,
-                                    int per, int32_t *__restrict__ idx, float *__restrict__ gate) {
-    extern __shared__ float tile[];  // [blockDim.x][N+1]
-    const int tpb = blockDim.x;
-    const int64_t t0 = (int64_t)blockIdx.x * tpb;
-    const int ntok = (int)min((int64_t)tpb, (int64_t)T - t0);
+constexpr int kSelectThreads = 128;
+constexpr int kSelectRows = 64;  // tokens per block (32 when N > 639, to fit the score tile)
+
+__global__ void __launch_bounds__(kSelectThreads)
+route_select_kernel(const float *__restrict__ logits, int T, int N, int groups, int G, int per, int rows_pb,
+                    int32_t *__restrict__ idx, float *__restrict__ gate) {
+    extern __shared__ float tile[];  // [rows_pb][N+1]
+    __shared__ float row_max[kSelectRows], row_sum[kSelectRows];
+    pdl_wait();
+    pdl_trigger();
+    const int64_t t0 = (int64_t)blockIdx.x * rows_pb;
+    const int ntok = (int)min((int64_t)rows_pb, (int64_t)T - t0);
     const int stride = N + 1;
     const float *src = logits + t0 * N;
-    for (int i = threadIdx.x; i < ntok * N; i += tpb) {
+    for (int i = threadIdx.x; i < ntok * N; i += kSelectThreads) {
         const int r = i / N, c = i - r * N;
         tile[r * stride + c] = src[i];
     }
     __syncthreads();
-    if (threadIdx.x < ntok) {
-        const int K = groups * per;
-        const int64_t t = t0 + threadIdx.x;
-        route_token(tile + threadIdx.x * stride, N, groups, G, per, idx + t * K, gate + t * K);
-    }
+    const int K = groups * per;
+    route_rows_block(tile, stride, 0, ntok, N, groups, G, per, idx + t0 * K, gate + t0 * K, row_max, row_sum);
 }
-
-static int route_tokens_per_block(int64_t N) { return (N <= 639) ? 64 : 32; }
 
 cudaError_t launch_route_select(const float *logits, int64_t T, int64_t N, int64_t M, int64_t kpg,
                                 bool global, int32_t *idx, float *gate, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const int tpb = route_tokens_per_block(N);
-    const size_t smem = (size_t)tpb * (N + 1) * sizeof(float);
+    const int rows_pb = N <= 639 ? kSelectRows : kSelectRows / 2;
+    const size_t smem = (size_t)rows_pb * (N + 1) * sizeof(float);
     cudaError_t err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
     const int groups = global ? 1 : (int)M;
     const int G = global ? (int)N : (int)(N / M);
     const int per = global ? (int)(M * kpg) : (int)kpg;
-    route_select_kernel<<<(unsigned)cdiv(T, tpb), tpb, smem, s>>>(logits, (int)T, (int)N, groups, G, per,
-                                                                   idx, gate);
+    err = launch_pdl(route_select_kernel, dim3((unsigned)cdiv(T, rows_pb)), dim3(kSelectThreads), smem, s,
+                     logits, (int)T, (int)N, groups, G, per, rows_pb, idx, gate);
     count_launches(1);
-    return cudaGetLastError();
+    return err;
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -6,13 +6,14 @@
 // handful of SMs idle.  Here every CTA computes the scores of kTokTile tokens x kExpTile experts
 // over the full hidden size (its threads split the hidden dimension, 16-byte loads, one round of
 // loads in flight, fixed summation order), writes them to the workspace and takes a ticket; the
-// last CTA to finish (no CTA ever waits) adds the bias and routes every token with one warp per
-// token -- global softmax, then group top-K' (Pangu Pro MoE explainer, section 1: scores for all
-// experts, one softmax over them, a local top-K' per group) -- and, when asked, permutes all
-// tokens in the same block (histogram, prefix sum, deterministic scatter, group loads and
-// imbalance score).
+// last CTA to finish (no CTA ever waits) adds the bias and routes every token with the whole
+// block (route_rows_block: global softmax, then group top-K' -- Pangu Pro MoE explainer, section
+// 1: scores for all experts, one softmax over them, a local top-K' per group) and, when asked,
+// permutes all tokens in the same block (histogram, prefix sum, deterministic scatter, group
+// loads and imbalance score).
 #include "common.cuh"
 #include "permute_block.cuh"
+#include "route_token.cuh"
 
 namespace moge {
 namespace rs {
@@ -20,8 +21,6 @@ namespace rs {
 constexpr int kThreads = kPermuteChunk;  // the permutation runs on one block of kPermuteChunk threads
 constexpr int kTokTile = 4;              // tokens per CTA
 constexpr int kExpTile = 8;              // experts per CTA
-constexpr int kRegGroup = 16;            // groups of up to this many experts are ranked in registers
-constexpr int kMaxRegGroups = 16;        // ... when there are at most this many groups
 
 struct Params {
     const void *x;        // [T, d]
@@ -57,28 +56,11 @@ __device__ __forceinline__ void unpack(const uint4 &v, float (&f)[4], float) {
     f[3] = __uint_as_float(v.w);
 }
 
-// Softmax normaliser of one token with a whole warp from its scores l[0..N) in shared memory:
-// m = max_e l[e] and s = sum_e exp(l[e] - m) by butterfly reductions.
-__device__ __forceinline__ void softmax_stats_warp(const float *l, int N, float &m_out, float &s_out) {
-    const int lane = threadIdx.x & 31;
-    float m = -__int_as_float(0x7f800000);
-    for (int e = lane; e < N; e += 32) m = fmaxf(m, l[e]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float s = 0.f;
-    for (int e = lane; e < N; e += 32) s += expf(l[e] - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    m_out = m;
-    s_out = s;
-}
-
 template <typename E>
 __global__ void __launch_bounds__(kThreads) route_small_kernel(const Params p) {
     extern __shared__ float sm[];
     __shared__ float part[kThreads / 32][kTokTile * kExpTile];
     __shared__ float tmax[kSmallRouteMaxT], tsum[kSmallRouteMaxT];
-    __shared__ float tpart[kSmallRouteMaxT * kMaxRegGroups], tpart2[kSmallRouteMaxT * kMaxRegGroups];
     __shared__ int is_last;
     constexpr int V = 16 / sizeof(E);  // elements per 16-byte vector
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,79 +154,7 @@ __global__ void __launch_bounds__(kThreads) route_small_kernel(const Params p) {
         if (p.logits) p.logits[i] = v;
     }
     __syncthreads();
-    if (p.G <= kRegGroup && p.groups <= kMaxRegGroups) {
-        // one thread per (token, group): the group's scores live in registers
-        const int pairs = p.T * p.groups;
-        for (int q = threadIdx.x; q < pairs; q += kThreads) {
-            const int t = q / p.groups, g = q - t * p.groups;
-            const float *l = stage + t * p.N + g * p.G;
-            float gm = -__int_as_float(0x7f800000);
-#pragma unroll
-            for (int j = 0; j < kRegGroup; ++j)
-                if (j < p.G) gm = fmaxf(gm, l[j]);
-            tpart[q] = gm;
-        }
-        __syncthreads();
-        for (int q = threadIdx.x; q < pairs; q += kThreads) {
-            const int t = q / p.groups, g = q - t * p.groups;
-            const float *l = stage + t * p.N + g * p.G;
-            float m = tpart[t * p.groups];
-            for (int h = 1; h < p.groups; ++h) m = fmaxf(m, tpart[t * p.groups + h]);
-            float v[kRegGroup];
-            float gs = 0.f;
-#pragma unroll
-            for (int j = 0; j < kRegGroup; ++j) {
-                v[j] = j < p.G ? l[j] : 0.f;
-                if (j < p.G) gs += expf(v[j] - m);
-            }
-            tpart2[q] = gs;
-            // rank of every member: #{members above it, or equal with a lower index}
-#pragma unroll
-            for (int j = 0; j < kRegGroup; ++j) {
-                if (j >= p.G) break;
-                int rank = 0;
-#pragma unroll
-                for (int i = 0; i < kRegGroup; ++i)
-                    if (i < p.G) rank += (v[i] > v[j]) || (v[i] == v[j] && i < j);
-                if (rank < p.per) sidx[t * K + g * p.per + rank] = g * p.G + j;
-            }
-            tmax[t] = m;  // every group of the token writes the same value
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < p.T * K; i += kThreads) {
-            const int t = i / K;
-            float s = tpart2[t * p.groups];
-            for (int h = 1; h < p.groups; ++h) s += tpart2[t * p.groups + h];
-            p.gate[i] = expf(stage[t * p.N + sidx[i]] - tmax[t]) / s;
-        }
-    } else {
-        // wide groups: statistics with one warp per token, ranks with one thread per (token, expert)
-        for (int t = warp; t < p.T; t += kThreads / 32) {
-            float m, sum;
-            softmax_stats_warp(stage + t * p.N, p.N, m, sum);
-            if (lane == 0) {
-                tmax[t] = m;
-                tsum[t] = sum;
-            }
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < p.T * p.N; i += kThreads) {
-            const int t = i / p.N, e = i - t * p.N;
-            const float *l = stage + t * p.N;
-            const int g = e / p.G, b = g * p.G;
-            const float v = l[e];
-            int rank = 0;
-            for (int j = b; j < b + p.G; ++j) {
-                const float u = l[j];
-                rank += (u > v) || (u == v && j < e);
-            }
-            if (rank < p.per) {
-                const int slot = t * K + g * p.per + rank;
-                sidx[slot] = e;
-                p.gate[slot] = expf(v - tmax[t]) / tsum[t];
-            }
-        }
-    }
+    route_rows_block(stage, p.N, 0, p.T, p.N, p.groups, p.G, p.per, sidx, p.gate, tmax, tsum);
     __syncthreads();
     for (int i = threadIdx.x; i < p.T * K; i += kThreads) p.idx[i] = sidx[i];
     if (p.counts)

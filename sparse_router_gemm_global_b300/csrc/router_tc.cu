@@ -5,12 +5,11 @@
 //
 // One CTA per (128-token tile, slice of the reduction over d).  128 threads: thread 0 of warp 0
 // issues TMA loads, thread 0 of warp 1 issues the MMAs (M = 128 tokens, N = N rounded up to 16
-// experts), then all four warps drain TMEM (warp w owns TMEM lanes 32w..32w+31 = token rows).
-// With one slice the CTA stages its fp32 scores in shared memory and routes its tokens.  With
-// S > 1 slices (small batches, so that more SMs stream W_r) every CTA writes its partial sums
-// to the workspace; the last CTA of a tile to finish (a counter in the workspace status page,
-// reset by that CTA) adds the S partials in slice order -- so the result does not depend on
-// which CTA finishes last -- and routes the tile.  No CTA waits on another.
+// experts), then all four warps drain TMEM (warp w owns TMEM lanes 32w..32w+31 = token rows)
+// into shared memory.  The S slices of a tile form one thread-block cluster: after a cluster
+// barrier, CTA j adds the S partial tiles for its share of the 128 tokens through distributed
+// shared memory, in slice order (so the result does not depend on timing), and routes those
+// tokens.  No CTA waits on a counter and nothing goes through global memory.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -27,6 +26,7 @@ constexpr int kThreads = 128;
 constexpr int kBM = kRouterTileRows;   // tokens per tile (MMA M)
 constexpr int kBK = 64;                // bf16 elements per k-block (one 128-byte swizzle row)
 constexpr int kMaxStages = 8;
+constexpr int kMaxSlices = 8;          // slices of a tile = CTAs of its cluster (portable size)
 constexpr int kSmemBudget = 200 * 1024;
 
 struct Params {
@@ -37,8 +37,6 @@ struct Params {
     float *logits;     // optional [T, N] output
     int32_t *idx;      // [T, K]
     float *gate;       // [T, K]
-    float *partials;   // [tiles][kslices][128][N] when kslices > 1
-    uint32_t *tickets; // [tiles] when kslices > 1
     uint32_t *status;
 };
 
@@ -49,7 +47,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
     __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], tfull_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
-    __shared__ int is_last;
+    __shared__ float row_max[kBM], row_sum[kBM];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -119,7 +117,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
     }
     __syncwarp();
 
-    // ---- drain TMEM: thread = token row r of the tile
+    // ---- drain TMEM into this CTA's partial tile: thread = token row r, stage[r][N+1]
     bool ok = wait_bar(smem_u32(&tfull_bar), 0, abort_v, p.status);
     ok = __all_sync(0xffffffffu, ok) && !*abort_v;
     tc_fence_after();
@@ -127,8 +125,6 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
     const int stride = p.N + 1;
     float *stage = reinterpret_cast<float *>(smem);  // [128][N+1], reuses the pipeline buffers
     const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-    float *my_partial = p.kslices > 1
-        ? p.partials + (((size_t)tile * p.kslices + slice) * kBM + r) * p.N : nullptr;
     for (int c0 = 0; c0 < p.npad; c0 += 16) {
         uint32_t v[16];
         if (ok) {
@@ -138,96 +134,61 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0u;
         }
-        if (r < ntok) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int c = c0 + j;
-                if (c < p.N) {
-                    if (my_partial) my_partial[c] = __uint_as_float(v[j]);
-                    else stage[r * stride + c] = __uint_as_float(v[j]);
-                }
-            }
+        for (int j = 0; j < 16; ++j) {
+            const int c = c0 + j;
+            if (c < p.N) stage[r * stride + c] = __uint_as_float(v[j]);
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
 
-    if (p.kslices > 1) {
-        // the last slice CTA of this tile sums the partials in slice order
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t ticket = atomicAdd(&p.tickets[tile], 1u);
-            is_last = (ticket == (uint32_t)p.kslices - 1);
-            if (is_last) p.tickets[tile] = 0u;  // ready for the next call
+    // ---- the slices' partial tiles are summed in slice order; CTA `slice` takes the rows
+    // [slice * rows_per, (slice + 1) * rows_per) of the tile
+    const int S = p.kslices;
+    const int rows_per = (kBM + S - 1) / S;
+    const int r0 = slice * rows_per, r1 = min(kBM, r0 + rows_per);
+    if (S > 1) {
+        cluster_sync();  // every partial tile of the cluster is in shared memory
+        const uint32_t my_stage = smem_u32(stage);
+        for (int i = threadIdx.x; i < (r1 - r0) * p.N; i += kThreads) {
+            const int rr = r0 + i / p.N, c = i - (i / p.N) * p.N;
+            const uint32_t off = (uint32_t)(rr * stride + c) * 4u;
+            float v[kMaxSlices];  // all slices' loads in flight together, then added in slice order
+#pragma unroll
+            for (int q = 0; q < kMaxSlices; ++q)
+                v[q] = q < S ? ld_shared_cluster_f32(mapa_shared(my_stage + off, (uint32_t)q)) : 0.f;
+            float acc = v[0];
+#pragma unroll
+            for (int q = 1; q < kMaxSlices; ++q)
+                if (q < S) acc += v[q];
+            stage[rr * stride + c] = acc;  // rows [r0, r1) of this CTA are read by no other CTA
         }
-        __syncthreads();
-        if (!is_last) return;
-        __threadfence();
-        // Each thread owns up to kRed float4 of the tile and adds the slices in order s = 0..S-1;
-        // the kRed loads of one slice are independent, so they are in flight together.
-        constexpr int kRed = 16;
-        const float4 *base = reinterpret_cast<const float4 *>(p.partials + (size_t)tile * p.kslices * kBM * p.N);
-        const int n4 = ntok * p.N / 4;  // N is a multiple of 4 on this path
-        const size_t slice4 = (size_t)kBM * p.N / 4;
-        for (int i0 = threadIdx.x; i0 < n4; i0 += kThreads * kRed) {
-            float4 acc[kRed];
-#pragma unroll
-            for (int j = 0; j < kRed; ++j) {
-                const int i = i0 + j * kThreads;
-                acc[j] = i < n4 ? __ldcg(base + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            for (int s = 1; s < p.kslices; ++s) {
-#pragma unroll
-                for (int j = 0; j < kRed; ++j) {
-                    const int i = i0 + j * kThreads;
-                    if (i < n4) {
-                        const float4 v = __ldcg(base + s * slice4 + i);
-                        acc[j].x += v.x;
-                        acc[j].y += v.y;
-                        acc[j].z += v.z;
-                        acc[j].w += v.w;
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kRed; ++j) {
-                const int i = (i0 + j * kThreads) * 4;
-                if (i < n4 * 4) {
-                    const int rr = i / p.N, c = i - rr * p.N;  // 4 | N: the float4 stays in one row
-                    float *dst = stage + rr * stride + c;
-                    dst[0] = acc[j].x;
-                    dst[1] = acc[j].y;
-                    dst[2] = acc[j].z;
-                    dst[3] = acc[j].w;
-                }
-            }
-        }
-        __syncthreads();
     }
+    __syncthreads();
 
-    // ---- bias, optional scores output, softmax + selection
-    for (int i = threadIdx.x; i < ntok * p.N; i += kThreads) {
-        const int rr = i / p.N, c = i - rr * p.N;
+    // ---- bias, optional scores output, softmax + selection of this CTA's rows
+    const int rows = min(r1, ntok) - r0;
+    for (int i = threadIdx.x; i < max(rows, 0) * p.N; i += kThreads) {
+        const int rr = r0 + i / p.N, c = i - (i / p.N) * p.N;
         float v = stage[rr * stride + c];
         if (p.bias) v += p.bias[c];
         stage[rr * stride + c] = v;
         if (p.logits) p.logits[(size_t)(t0 + rr) * p.N + c] = v;
     }
     __syncthreads();
-    if (r < ntok) {
-        const int K = p.groups * p.per;
-        route_token(stage + r * stride, p.N, p.groups, p.G, p.per, p.idx + (size_t)(t0 + r) * K,
-                    p.gate + (size_t)(t0 + r) * K);
-    }
+    if (rows > 0)
+        route_rows_block(stage, stride, r0, r0 + rows, p.N, p.groups, p.G, p.per, p.idx + (size_t)t0 * (p.groups * p.per),
+                         p.gate + (size_t)t0 * (p.groups * p.per), row_max, row_sum);
+    if (S > 1) cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace rt
 
 cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, int64_t T, int64_t d, int64_t N,
                              int64_t M, int64_t kpg, bool global, float *logits_out, int32_t *idx, float *gate,
-                             float *partials, uint32_t *tickets, uint32_t *status, cudaStream_t s) {
+                             uint32_t *status, cudaStream_t s) {
     using namespace rt;
     if (T == 0) return cudaSuccess;
     if (N > 256) return cudaErrorInvalidValue;
@@ -255,8 +216,6 @@ cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, 
     p.logits = logits_out;
     p.idx = idx;
     p.gate = gate;
-    p.partials = partials;
-    p.tickets = tickets;
     p.status = status;
     const size_t stage_floats = (size_t)kBM * (N + 1) * 4;
     size_t smem = std::max((size_t)p.stages * p.stage_bytes, stage_floats) + 1024;
@@ -284,8 +243,22 @@ cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, 
     }
     cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    dim3 grid((unsigned)cdiv(T, kBM), (unsigned)p.kslices);
-    err = launch_pdl(router_tc_kernel, grid, dim3(kThreads), smem, s, mx, mw, p);
+    // the slices of a tile form one cluster (1 x kslices)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)cdiv(T, kBM), (unsigned)p.kslices);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = (unsigned)p.kslices;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    err = cudaLaunchKernelEx(&cfg, router_tc_kernel, mx, mw, p);
     count_launches(1);
     return err;
 }

@@ -161,6 +161,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
+// Load a float from the shared memory of a CTA of the cluster (shared::cluster address).
+// (Ordered after a preceding cluster barrier, which is an asm volatile statement too.)
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
+    return v;
+}
+
 // All threads of both CTAs: release this CTA's prior shared-memory writes, acquire the peer's.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
