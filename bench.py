@@ -604,34 +604,40 @@ def run_reference(args):
 # DRAM traffic of the grouped GEMM from an ncu capture (profiles/ncu_traffic.json)
 # --------------------------------------------------------------------------------------------
 
-TRAFFIC_KERNELS = {  # part of the ncu kernel name -> record key
-    "ffn_tc_pair_kernel<1>": "prefill_t8192:gate_up",
-    "ffn_tc_pair_kernel<0>": "prefill_t8192:down",
-    "ffn_tc_kernel<2, 32, 1>": "decode_t32:gate_up",
-    "ffn_tc_kernel<3, 32, 0>": "decode_t32:down",
+TRAFFIC_KERNELS = {  # part of the ncu kernel name -> (record key, counts the stage's launches)
+    "ffn_tc_pair_kernel<1>": ("prefill_t8192:gate_up", True),
+    "ffn_tc_kernel<0, 0, 0>": ("prefill_t8192:gate_up", False),  # short-block remainder of gate/up
+    "ffn_tc_pair_kernel<0>": ("prefill_t8192:down", True),
+    "ffn_tc_kernel<1, 0, 0>": ("prefill_t8192:down", False),     # short-block remainder of down
+    "ffn_tc_kernel<2, 32, 1>": ("decode_t32:gate_up", True),
+    "ffn_tc_kernel<3, 32, 0>": ("decode_t32:down", True),
 }
 
 
 def record_traffic(csv_path: str, command: str) -> None:
-    """Median dram__bytes_read.sum + dram__bytes_write.sum per launch of each grouped-GEMM kernel
-    in an ncu --csv capture of this bench at full size, stamped with the kernel source hash."""
+    """dram__bytes_read.sum + dram__bytes_write.sum per stage of each grouped GEMM in an ncu --csv
+    capture of this bench at full size, stamped with the kernel source hash.  A stage is one launch
+    of its main kernel plus, for the prefill, one launch of the short-block remainder kernel: the
+    stage's bytes are the total over both kernels divided by the main kernel's launches."""
     import csv
-    per = {}
+    total, launches = {}, {}
     with open(csv_path) as f:
         rows = [r for r in csv.reader(f) if len(r) > 10]
     hdr = rows[0]
     ki, ii, mi, vi = (hdr.index(k) for k in ("Kernel Name", "ID", "Metric Name", "Metric Value"))
     for r in rows[1:]:
-        key = next((v for k, v in TRAFFIC_KERNELS.items() if k in r[ki]), None)
-        if key is None or not r[mi].startswith("dram__bytes_"):
+        hit = next((v for k, v in TRAFFIC_KERNELS.items() if k in r[ki]), None)
+        if hit is None or not r[mi].startswith("dram__bytes_"):
             continue
-        per.setdefault(key, {}).setdefault(r[ii], 0.0)
-        per[key][r[ii]] += float(r[vi].replace(",", ""))
+        key, main_kernel = hit
+        total[key] = total.get(key, 0.0) + float(r[vi].replace(",", ""))
+        if main_kernel:
+            launches.setdefault(key, set()).add(r[ii])
     rec = {"command": command, "kernel_sha256_16": kernel_hash()}
-    for key, launches in per.items():
-        vals = sorted(launches.values())
-        rec[key] = {"kernel_sha256_16": kernel_hash(), "launches": len(vals),
-                    "dram_bytes_per_launch": vals[len(vals) // 2]}
+    for key in total:
+        n = len(launches.get(key, ()))
+        if n:
+            rec[key] = {"kernel_sha256_16": kernel_hash(), "launches": n, "dram_bytes_per_launch": total[key] / n}
     with open(TRAFFIC_PATH, "w") as f:
         json.dump(rec, f, indent=1)
     print(json.dumps(rec, indent=1))
