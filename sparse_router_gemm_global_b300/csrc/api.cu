@@ -182,7 +182,7 @@ moge_status_t layer_impl(const moge_config_t *cfg, int64_t S, const void *x, con
     const bool gather_in_gemm = gathers_in_gemm(*cfg, S);
     mark_stage(MOGE_STAGE_GATHER, st);
     if (e == cudaSuccess && !gather_in_gemm)
-        e = launch_gather_rows(x, row_token, offsets, cfg->N + S, rows, cfg->d, cfg->act_dtype, x_perm, st);
+        e = launch_scatter_rows(x, pair_row, cfg->T, K, S, P, cfg->d, cfg->act_dtype, x_perm, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark_stage(MOGE_STAGE_GATE_UP, st);  // the FFN marks MOGE_STAGE_DOWN between its two GEMMs
     s = gather_in_gemm ? ffn_impl(cfg, x, row_token, offsets, w_gate, w_up, w_down, y_perm, ws, st, S)
@@ -268,8 +268,10 @@ moge_status_t moge_permute(const moge_config_t *cfg, const int32_t *topk_idx, co
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = launch_permute(topk_idx, cfg->T, K, cfg->N, counts, offsets, pair_row, row_token,
                                    at<int32_t>(ws, L.chunk_counts), at<uint32_t>(ws, L.status), st);
-    if (e == cudaSuccess && gather)
-        e = launch_gather_rows(x, row_token, offsets, cfg->N, cfg->T * K, cfg->d, cfg->act_dtype, x_perm, st);
+    if (e == cudaSuccess && gather)  // token-major copy when the slot -> row map is an output
+        e = pair_row ? launch_scatter_rows(x, pair_row, cfg->T, K, 0, 0, cfg->d, cfg->act_dtype, x_perm, st)
+                     : launch_gather_rows(x, row_token, offsets, cfg->N, cfg->T * K, cfg->d, cfg->act_dtype,
+                                          x_perm, st);
     return cuda_status(e);
 }
 

@@ -191,6 +191,9 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
                            float *score = nullptr);
 cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const int32_t *offsets,
                                int64_t N, int64_t P, int64_t d, int dtype, void *x_perm, cudaStream_t s);
+// x_perm[pair_row[t,k]] = x[t] (k < K) and x_perm[shared_base + s*T + t] = x[t] (s < S).
+cudaError_t launch_scatter_rows(const void *x, const int32_t *pair_row, int64_t T, int64_t K, int64_t S,
+                                int64_t shared_base, int64_t d, int dtype, void *x_perm, cudaStream_t s);
 cudaError_t launch_imbalance(const int32_t *counts, int64_t T, int64_t N, int64_t M, int32_t *group_load,
                              float *score, cudaStream_t s);
 // y[t] = sum_k gate[t,k] * y_perm[pair_row[t,k]] + sum_{s<S} y_perm[shared_base + s*T + t]

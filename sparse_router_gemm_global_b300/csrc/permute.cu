@@ -202,6 +202,76 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *row_token, const in
 }
 
 // ---------------------------------------------------------------------------------------------
+// Token-major row copy: x_perm[pair_row[t,k],:] = x[t,:] for every slot k, and
+// x_perm[shared_base + s*T + t,:] = x[t,:] for each of S shared experts.  The same rows as the
+// gather above, but a warp loads one 32 x kBatch-vector chunk of a token's row once and stores it
+// to all its destinations, so the copy reads x about once whatever L2 keeps.  Work item =
+// (token, chunk, destination group): small batches split the K + S destinations of a token into
+// `dgroups` groups so that enough warps are in flight; one warp per item.
+// ---------------------------------------------------------------------------------------------
+constexpr int kScatterBatch = 8;
+constexpr int64_t kScatterChunkVec = 32 * kScatterBatch;
+constexpr int kScatterThreads = 128;
+
+__global__ void __launch_bounds__(kScatterThreads)
+scatter_rows_kernel(const int4 *__restrict__ x, const int32_t *__restrict__ pair_row, int64_t T, int K, int S,
+                    int64_t shared_base, int64_t vec_per_row, int dgroups, int4 *__restrict__ x_perm) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t chunks = (vec_per_row + kScatterChunkVec - 1) / kScatterChunkVec;
+    const int64_t items = T * chunks * dgroups;
+    const int dests = K + S;
+    const int per = (dests + dgroups - 1) / dgroups;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t item = warp; item < items; item += nwarps) {
+        const int64_t tc = item / dgroups;
+        const int g = (int)(item - tc * dgroups);
+        const int64_t t = tc / chunks;
+        const int64_t v0 = (tc - t * chunks) * kScatterChunkVec + lane;
+        const int4 *src = x + t * vec_per_row;
+        int4 buf[kScatterBatch];
+#pragma unroll
+        for (int j = 0; j < kScatterBatch; ++j) {
+            const int64_t v = v0 + 32 * j;
+            if (v < vec_per_row) buf[j] = __ldg(src + v);
+        }
+        const int32_t *pr = pair_row + t * K;
+        const int k1 = min(dests, (g + 1) * per);
+        for (int k = g * per; k < k1; ++k) {
+            const int64_t r = k < K ? (int64_t)__ldg(pr + k) : shared_base + (int64_t)(k - K) * T + t;
+            int4 *dst = x_perm + r * vec_per_row;
+#pragma unroll
+            for (int j = 0; j < kScatterBatch; ++j) {
+                const int64_t v = v0 + 32 * j;
+                if (v < vec_per_row) __stcs(dst + v, buf[j]);
+            }
+        }
+    }
+}
+
+cudaError_t launch_scatter_rows(const void *x, const int32_t *pair_row, int64_t T, int64_t K, int64_t S,
+                                int64_t shared_base, int64_t d, int dtype, void *x_perm, cudaStream_t s) {
+    const int64_t dests = K + S;
+    if (T == 0 || dests == 0) return cudaSuccess;
+    const int64_t vec = d * (dtype == MOGE_BF16 ? 2 : 4) / 16;
+    int sms = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t base_items = T * cdiv(vec, kScatterChunkVec);
+    const int64_t want = (int64_t)sms * 16;  // warps to keep in flight
+    const int dgroups = (int)std::min<int64_t>(dests, std::max<int64_t>(1, cdiv(want, base_items)));
+    const int64_t warps_per_block = kScatterThreads / 32;
+    const unsigned blocks =
+        (unsigned)std::min<int64_t>(cdiv(base_items * dgroups, warps_per_block), (int64_t)1 << 30);
+    cudaError_t err = launch_pdl(scatter_rows_kernel, dim3(blocks), dim3(kScatterThreads), 0, s, (const int4 *)x,
+                                 pair_row, T, (int)K, (int)S, shared_base, vec, dgroups, (int4 *)x_perm);
+    count_launches(1);
+    return err;
+}
+
+// ---------------------------------------------------------------------------------------------
 // Shared experts: every token visits each of the S shared experts, so their rows are fixed:
 // expert N + s owns rows [P + s*T, P + (s+1)*T), row P + s*T + t holding token t.
 // ---------------------------------------------------------------------------------------------

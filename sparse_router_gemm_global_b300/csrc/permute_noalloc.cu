@@ -76,6 +76,7 @@ extern "C" moge_status_t moge_permute_noalloc(const moge_config_t *cfg, const in
     cudaError_t e = launch_permute(topk_idx, c.T, K, c.N, counts, offsets, pair_row, row_token, scratch,
                                    nullptr, st);
     if (e == cudaSuccess && gather)
-        e = launch_gather_rows(x, row_token, offsets, c.N, c.T * K, c.d, c.act_dtype, x_perm, st);
+        e = pair_row ? launch_scatter_rows(x, pair_row, c.T, K, 0, 0, c.d, c.act_dtype, x_perm, st)
+                     : launch_gather_rows(x, row_token, offsets, c.N, c.T * K, c.d, c.act_dtype, x_perm, st);
     return e == cudaSuccess ? MOGE_OK : MOGE_ERR_CUDA;
 }

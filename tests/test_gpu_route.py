@@ -86,23 +86,36 @@ def test_one_expert_takes_every_token():
     assert got["counts"][5] == T
 
 
-def test_permute_gathers_rows_exactly():
-    w = synth.WORKLOADS["decode_t32"].with_(T=700, d=256)
-    x = synth.normal(3, synth.TID_X, (w.T, w.d), 1.0, "bf16")
+@pytest.mark.parametrize("T,d,dtype", [
+    (700, 256, "bf16"),    # one 32-vector chunk per row, destinations split in 4 groups per token
+    (5, 4104, "bf16"),     # rows of 513 vectors: three chunks, the last ragged; 16 destination groups
+    (3000, 4104, "bf16"),  # one destination group
+    (300, 1028, "f32"),    # fp32 rows, ragged chunk
+])
+@pytest.mark.parametrize("with_pair_row", [True, False])
+def test_permute_gathers_rows_exactly(T, d, dtype, with_pair_row):
+    """x_perm[r] = x[row_token[r]] bit for bit: the token-major copy when pair_row is an output, the
+    row-major gather through row_token when it is not."""
+    w = synth.WORKLOADS["decode_t32"].with_(T=T, d=d)
+    x = synth.normal(3, synth.TID_X, (w.T, w.d), 1.0, dtype)
     l = synth.route_logits(4, w.T, w.N)
     ref = oracle.route(l, w.M, w.kpg)
-    c = moge.make_config(w.T, w.d, w.N, w.M, w.kpg, w.I, "bf16")
+    c = moge.make_config(w.T, w.d, w.N, w.M, w.kpg, w.I, dtype)
     ws = moge.alloc_workspace(c)
     idx = dev(ref["idx"])
     counts = torch.empty(w.N, dtype=torch.int32, device=DEV)
     offsets = torch.empty(w.N + 1, dtype=torch.int32, device=DEV)
-    pair_row = torch.empty((w.T, w.K), dtype=torch.int32, device=DEV)
+    pair_row = torch.empty((w.T, w.K), dtype=torch.int32, device=DEV) if with_pair_row else None
     row_token = torch.empty(w.P, dtype=torch.int32, device=DEV)
-    x_perm = torch.empty((w.P, w.d), dtype=torch.bfloat16, device=DEV)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x_perm = torch.full((w.P, w.d), 7.0, dtype=tdt, device=DEV)
     moge.moge_permute(c, idx, dev(x), counts, offsets, pair_row, row_token, x_perm, ws)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(host(pair_row), ref["pair_row"])
-    np.testing.assert_array_equal(host(x_perm), x[ref["row_token"]])
+    perm = oracle.permute(ref["idx"], w.N)
+    if with_pair_row:
+        np.testing.assert_array_equal(host(pair_row), perm["pair_row"])
+    np.testing.assert_array_equal(host(row_token), perm["row_token"])
+    np.testing.assert_array_equal(host(x_perm), x[perm["row_token"]])
 
 
 def test_empty_batch():
