@@ -142,12 +142,15 @@ moge_status_t moge_route(const moge_config_t *cfg, moge_route_mode_t mode, const
  *   pair_row[t,k] = offsets[e] + #{t' < t routed to e}, e = topk_idx[t,k]
  *   row_token[r]  = token of row r
  *   x_perm[r,:]   = x[row_token[r],:]   (skipped when x or x_perm is NULL)
- * row_token and pair_row may be NULL when not wanted. */
+ * row_token and pair_row may be NULL when not wanted, except that x_perm needs
+ * row_token.  With pair_row given the copy runs token by token (each row of x
+ * is read once and stored to the rows of its pairs); without it, row by row
+ * through row_token.  Rows r >= offsets[N] of x_perm are not written. */
 moge_status_t moge_permute(const moge_config_t *cfg, const int32_t *topk_idx, const void *x,
                            int32_t *counts, int32_t *offsets, int32_t *pair_row, int32_t *row_token,
                            void *x_perm, void *ws, size_t ws_bytes, moge_stream_t stream);
 
-/* moge_permute without a workspace.  The paper has no counterpart: this entry
+/* moge_permute without a workspace.  The method has no counterpart: this entry
  * point exists for callers that cannot allocate device memory (a serving
  * runtime whose pool already owns all of HBM and hands a plugin only its input
  * and output buffers, or a latency-critical loop that must not call cudaMalloc,

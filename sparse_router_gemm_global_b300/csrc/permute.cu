@@ -241,6 +241,7 @@ scatter_rows_kernel(const int4 *__restrict__ x, const int32_t *__restrict__ pair
         const int k1 = min(dests, (g + 1) * per);
         for (int k = g * per; k < k1; ++k) {
             const int64_t r = k < K ? (int64_t)__ldg(pr + k) : shared_base + (int64_t)(k - K) * T + t;
+            if (r < 0) continue;  // a slot whose expert id the permutation skipped owns no row
             int4 *dst = x_perm + r * vec_per_row;
 #pragma unroll
             for (int j = 0; j < kScatterBatch; ++j) {

@@ -118,6 +118,52 @@ def test_permute_gathers_rows_exactly(T, d, dtype, with_pair_row):
     np.testing.assert_array_equal(host(x_perm), x[perm["row_token"]])
 
 
+@pytest.mark.parametrize("with_pair_row", [True, False])
+def test_permute_skips_out_of_range_ids_and_writes_nothing_else(with_pair_row):
+    """Ids outside [0, N) own no row: pair_row = -1 there, the other pairs keep the order of the
+    definition, and the row copy writes rows [0, valid pairs) only.  x_perm is a view one row into
+    a larger buffer, so a store to row -1 or past the last row would show in the guard rows."""
+    T, d, N, M, kpg = 300, 264, 16, 4, 1
+    w = synth.WORKLOADS["decode_t32"].with_(T=T, d=d, N=N, M=M, kpg=kpg)
+    x = synth.normal(5, synth.TID_X, (T, d), 1.0, "bf16")
+    idx = oracle.route(synth.route_logits(6, T, N), M, kpg)["idx"].copy()
+    bad = np.random.default_rng(1).random(idx.shape) < 0.2
+    idx[bad] = np.resize(np.array([-1, N, 1000, -7], dtype=np.int32), int(bad.sum()))
+    # the definition on the valid pairs, in (token, slot) order
+    valid = (idx >= 0) & (idx < N)
+    counts = np.bincount(idx[valid], minlength=N).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    pair_row_ref = np.full(idx.shape, -1, dtype=np.int32)
+    fill = offsets[:-1].copy()
+    for t in range(T):
+        for k in range(w.K):
+            e = idx[t, k]
+            if 0 <= e < N:
+                pair_row_ref[t, k] = fill[e]
+                fill[e] += 1
+    pv = int(offsets[N])
+    row_token_ref = np.empty(pv, dtype=np.int32)
+    row_token_ref[pair_row_ref[valid]] = np.nonzero(valid)[0]
+    c = moge.make_config(T, d, N, M, kpg, 64, "bf16")
+    ws = moge.alloc_workspace(c)
+    cnt = torch.empty(N, dtype=torch.int32, device=DEV)
+    off = torch.empty(N + 1, dtype=torch.int32, device=DEV)
+    pair_row = torch.empty((T, w.K), dtype=torch.int32, device=DEV) if with_pair_row else None
+    row_token = torch.full((T * w.K,), -9, dtype=torch.int32, device=DEV)
+    buf = torch.full((T * w.K + 2, d), 3.0, dtype=torch.bfloat16, device=DEV)
+    moge.moge_permute(c, dev(idx), dev(x), cnt, off, pair_row, row_token, buf[1:], ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(cnt), counts)
+    np.testing.assert_array_equal(host(off), offsets)
+    if with_pair_row:
+        np.testing.assert_array_equal(host(pair_row), pair_row_ref)
+    np.testing.assert_array_equal(host(row_token)[:pv], row_token_ref)
+    got = host(buf)
+    np.testing.assert_array_equal(got[1:pv + 1], x[row_token_ref])
+    guard = host(torch.full((1, d), 3.0, dtype=torch.bfloat16))
+    assert np.all(got[0] == guard[0]) and np.all(got[pv + 1:] == guard[0])
+
+
 def test_empty_batch():
     c = moge.make_config(0, 0, 16, 4, 1, 0, "f32")
     ws = moge.alloc_workspace(c)
