@@ -179,7 +179,11 @@ moge_status_t moge_permute_noalloc(const moge_config_t *cfg, const int32_t *topk
  *   h[r,:]      = silu(x_perm[r,:] W_gate[e]^T) * (x_perm[r,:] W_up[e]^T)
  *   y_perm[r,:] = h[r,:] W_down[e]^T
  * with fp32 accumulation; for bf16, h is rounded to bf16 before the down
- * projection and y_perm is bf16.  `offsets` is read on the device only.
+ * projection and y_perm is bf16.  `offsets` is read on the device only; it
+ * should hold 0 <= offsets[0] <= ... <= offsets[N] <= P (P = T*K), as
+ * moge_permute writes it.  Segments outside [0, P) are clamped to it, so no
+ * offsets make the call touch a row outside x_perm, h or y_perm; rows that no
+ * segment covers are left unwritten.
  * Needs ws (h lives there). */
 moge_status_t moge_expert_ffn(const moge_config_t *cfg, const void *x_perm, const int32_t *offsets,
                               const void *w_gate, const void *w_up, const void *w_down, void *y_perm,
@@ -187,7 +191,8 @@ moge_status_t moge_expert_ffn(const moge_config_t *cfg, const void *x_perm, cons
 
 /* Weighted combine in fixed slot order with fp32 accumulation:
  *   y[t,:] = sum_{k=0..K-1} topk_gate[t,k] * y_perm[pair_row[t,k],:]
- * rounded once to the activation dtype. */
+ * rounded once to the activation dtype.  A pair_row entry outside [0, T*K)
+ * (moge_permute writes -1 for a skipped expert id) is an absent slot. */
 moge_status_t moge_combine(const moge_config_t *cfg, const void *y_perm, const int32_t *pair_row,
                            const float *topk_gate, void *y, moge_stream_t stream);
 

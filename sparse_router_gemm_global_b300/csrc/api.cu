@@ -135,7 +135,6 @@ moge_status_t layer_impl(const moge_config_t *cfg, int64_t S, const void *x, con
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t K = cfg->M * cfg->k_per_group;
     const int64_t P = cfg->T * K;
-    const int64_t rows = P + S * cfg->T;
     if (cfg->T == 0) {  // empty batch: only the counts/offsets/score outputs exist
         if (a.counts || a.offsets || a.score || a.group_load) {
             int32_t *counts = a.counts ? a.counts : at<int32_t>(ws, L.counts);

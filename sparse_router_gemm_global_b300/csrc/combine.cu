@@ -1,6 +1,8 @@
 // Weighted combine: y[t,:] = sum_{k=0..K-1} gate[t,k] * y_perm[pair_row[t,k],:], summed in
 // slot order with fp32 accumulation and rounded once to the activation dtype; with S shared
 // experts their rows y_perm[shared_base + s*T + t,:] follow with weight 1, in order s = 0..S-1.
+// A pair_row entry outside [0, rows) (-1: the permutation skipped the slot's expert id) counts
+// as an absent slot.
 // Grid (token, column block): each thread owns one 16-byte column vector of one token and
 // issues the loads of 8 slots before their FMAs, so the reads of y_perm stay in flight
 // together instead of one round trip per slot.
@@ -14,7 +16,7 @@ constexpr int kSlotBatch = 8;
 template <typename T, int V>  // V elements per 16-byte vector
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_row, const float *__restrict__ gate,
-               int K, int64_t d, T *__restrict__ y, int S, int64_t shared_base, int64_t Tn) {
+               int K, int64_t d, T *__restrict__ y, int S, int64_t shared_base, int64_t Tn, int64_t rows) {
     pdl_wait();
     pdl_trigger();
     const int64_t t = blockIdx.x;
@@ -32,7 +34,8 @@ combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_ro
 #pragma unroll
         for (int j = 0; j < kSlotBatch; ++j) {
             const int k = k0 + j;
-            const int row = k < K ? __ldg(pr + k) : -1;  // -1: slot absent or id skipped by the permutation
+            int row = k < K ? __ldg(pr + k) : -1;
+            if (row >= rows) row = -1;
             g[j] = row >= 0 ? __ldg(gt + k) : 0.f;
             raw[j] = row >= 0 ? __ldg(reinterpret_cast<const int4 *>(y_perm + (int64_t)row * d) + v)
                               : make_int4(0, 0, 0, 0);
@@ -71,12 +74,13 @@ cudaError_t launch_combine(const void *y_perm, const int32_t *pair_row, const fl
     if (T == 0) return cudaSuccess;
     const int V = dtype == MOGE_BF16 ? 8 : 4;
     dim3 grid((unsigned)T, (unsigned)cdiv(d / V, kCombineThreads));
+    const int64_t rows = T * K + S * T;  // routed rows, then the shared experts' rows
     cudaError_t err = dtype == MOGE_BF16
         ? launch_pdl(combine_kernel<__nv_bfloat16, 8>, grid, dim3(kCombineThreads), 0, s,
                      (const __nv_bfloat16 *)y_perm, pair_row, gate, (int)K, d, (__nv_bfloat16 *)y, (int)S,
-                     shared_base, T)
+                     shared_base, T, rows)
         : launch_pdl(combine_kernel<float, 4>, grid, dim3(kCombineThreads), 0, s, (const float *)y_perm, pair_row,
-                     gate, (int)K, d, (float *)y, (int)S, shared_base, T);
+                     gate, (int)K, d, (float *)y, (int)S, shared_base, T, rows);
     count_launches(1);
     return err;
 }

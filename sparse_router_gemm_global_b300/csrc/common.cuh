@@ -62,6 +62,14 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 __host__ __device__ constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
+// First row and row count of expert e's segment [offsets[e], offsets[e+1]), clamped to the
+// buffer's rows [0, rows): offsets that no permutation wrote (decreasing, negative or past the
+// end) never lead a kernel to a row outside its buffers, nor to more tiles than the rows hold.
+__device__ __forceinline__ void expert_segment(const int32_t *offsets, int e, int rows, int &begin, int &count) {
+    begin = min(max(offsets[e], 0), rows);
+    count = min(max(offsets[e + 1], begin), rows) - begin;
+}
+
 // SwiGLU activation silu(a) * u with silu(a) = a / (1 + exp(-a)).
 // swiglu_fast uses the hardware exp2 approximation (bf16 tensor-core path, whose
 // output is rounded to bf16 anyway); swiglu_precise uses expf (all-fp32 path).

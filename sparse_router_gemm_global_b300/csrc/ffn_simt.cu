@@ -12,14 +12,17 @@ namespace moge {
 constexpr int kTile = 32;
 constexpr int kMaxExpertsSimt = 1024;
 
-// Map a linear tile id to (expert, row block).  tiles_before[e] in shared memory.
-__device__ __forceinline__ bool tile_to_expert(const int32_t *__restrict__ offsets, int N, int64_t row_tile,
-                                               int32_t *tiles_before, int *expert, int64_t *rb) {
+// Map a linear tile id to (expert, row block).  tiles_before[e] in shared memory; segments
+// clamped to the buffer's rows.
+__device__ __forceinline__ bool tile_to_expert(const int32_t *__restrict__ offsets, int N, int rows,
+                                               int64_t row_tile, int32_t *tiles_before, int *expert, int64_t *rb) {
     if (threadIdx.x == 0) {
         int64_t run = 0;
         for (int e = 0; e < N; ++e) {
             tiles_before[e] = (int32_t)run;
-            run += cdiv(offsets[e + 1] - offsets[e], kTile);
+            int begin, count;
+            expert_segment(offsets, e, rows, begin, count);
+            run += cdiv(count, kTile);
         }
         tiles_before[N] = (int32_t)run;
     }
@@ -37,7 +40,7 @@ __device__ __forceinline__ bool tile_to_expert(const int32_t *__restrict__ offse
 
 // out[r, c] for r in the expert's rows, c < OUT; A [P, Kd], W [N, OUT, Kd].
 template <typename T, bool GLU>
-__global__ void ffn_simt_kernel(const T *__restrict__ A, const int32_t *__restrict__ offsets, int N,
+__global__ void ffn_simt_kernel(const T *__restrict__ A, const int32_t *__restrict__ offsets, int N, int rows,
                                 const T *__restrict__ W0, const T *__restrict__ W1, int64_t Kd, int64_t OUT,
                                 T *__restrict__ out) {
     __shared__ int32_t tiles_before[kMaxExpertsSimt + 1];
@@ -46,9 +49,11 @@ __global__ void ffn_simt_kernel(const T *__restrict__ A, const int32_t *__restri
     __shared__ float w1s[GLU ? kTile : 1][kTile + 1];
     int e;
     int64_t rb;
-    if (!tile_to_expert(offsets, N, blockIdx.x, tiles_before, &e, &rb)) return;
-    const int64_t row0 = offsets[e] + rb * kTile;
-    const int64_t row_end = offsets[e + 1];
+    if (!tile_to_expert(offsets, N, rows, blockIdx.x, tiles_before, &e, &rb)) return;
+    int seg0, cnt;
+    expert_segment(offsets, e, rows, seg0, cnt);
+    const int64_t row0 = seg0 + rb * kTile;
+    const int64_t row_end = seg0 + cnt;
     const int64_t c0 = (int64_t)blockIdx.y * kTile;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 warps, 4 rows each
     const T *W0e = W0 + (int64_t)e * OUT * Kd;
@@ -91,11 +96,11 @@ static cudaError_t ffn_simt_typed(const T *x_perm, const int32_t *offsets, int64
                                   cudaStream_t s) {
     const int64_t row_tiles = cdiv(P, kTile) + N;  // upper bound of sum_e ceil(count_e / kTile)
     dim3 g1((unsigned)row_tiles, (unsigned)cdiv(I, kTile));
-    ffn_simt_kernel<T, true><<<g1, 256, 0, s>>>(x_perm, offsets, (int)N, wg, wu, d, I, h);
+    ffn_simt_kernel<T, true><<<g1, 256, 0, s>>>(x_perm, offsets, (int)N, (int)P, wg, wu, d, I, h);
     count_launches(1);
     mark_stage(MOGE_STAGE_DOWN, s);
     dim3 g2((unsigned)row_tiles, (unsigned)cdiv(d, kTile));
-    ffn_simt_kernel<T, false><<<g2, 256, 0, s>>>(h, offsets, (int)N, wd, nullptr, I, d, y_perm);
+    ffn_simt_kernel<T, false><<<g2, 256, 0, s>>>(h, offsets, (int)N, (int)P, wd, nullptr, I, d, y_perm);
     count_launches(1);
     return cudaGetLastError();
 }

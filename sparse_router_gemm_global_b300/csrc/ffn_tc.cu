@@ -97,11 +97,12 @@ struct Params {
     uint32_t *status;        // workspace status word
     const int32_t *row_token;  // [P] token of each permuted row (gathering launches only)
     int rule;                  // BlockRule of the tile list
+    int rows;                  // rows of the row buffers (act / out): segments are clamped to them
 };
 
 // prefix[e] = sum over e' < e of the row blocks of expert e' (BlockRule); all 256 threads, N <= 1024.
-__device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int tok_block, int rule, int32_t *prefix,
-                             int32_t *warp_sums) {
+__device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int rows, int tok_block, int rule,
+                             int32_t *prefix, int32_t *warp_sums) {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     int v[4];
     int local = 0;
@@ -109,7 +110,11 @@ __device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int tok
     for (int i = 0; i < 4; ++i) {
         const int e = t * 4 + i;
         int b = 0;
-        if (e < N) b = expert_blocks(offsets[e + 1] - offsets[e], tok_block, rule);
+        if (e < N) {
+            int begin, count;
+            expert_segment(offsets, e, rows, begin, count);
+            b = expert_blocks(count, tok_block, rule);
+        }
         local += b;
         v[i] = local;
     }
@@ -202,7 +207,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     }
     pdl_wait();  // the offsets (and the token rows) come from earlier kernels
     pdl_trigger();
-    build_prefix(p.offsets, p.N, C::tok_block, p.rule, prefix, warp_sums);  // contains __syncthreads
+    build_prefix(p.offsets, p.N, p.rows, C::tok_block, p.rule, prefix, warp_sums);  // contains __syncthreads
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -227,12 +232,14 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
             int e, tb, fb;
             tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
             int first, nrows;
-            block_rows(p.offsets[e + 1] - p.offsets[e], tb, C::tok_block, p.rule, first, nrows);
-            const int tok0 = p.offsets[e] + first;
+            int seg0, cnt;
+            expert_segment(p.offsets, e, p.rows, seg0, cnt);
+            block_rows(cnt, tb, C::tok_block, p.rule, first, nrows);
+            const int tok0 = seg0 + first;
             const int f0 = fb * C::feat_block;
             int r4[4] = {0, 0, 0, 0};
             if (gather_lane) {
-                const int last = p.offsets[e + 1] - 1;  // rows past the expert repeat its last row
+                const int last = seg0 + cnt - 1;  // rows past the expert repeat its last row
 #pragma unroll
                 for (int j = 0; j < 4; ++j) r4[j] = p.row_token[min(tok0 + lane * 4 + j, last)];
             }
@@ -334,8 +341,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
             int e, tb, fb;
             tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
             int first, ntok;  // ntok: valid token rows of this tile
-            block_rows(p.offsets[e + 1] - p.offsets[e], tb, C::tok_block, p.rule, first, ntok);
-            const int tok0 = p.offsets[e] + first;
+            int seg0, cnt;
+            expert_segment(p.offsets, e, p.rows, seg0, cnt);
+            block_rows(cnt, tb, C::tok_block, p.rule, first, ntok);
+            const int tok0 = seg0 + first;
             const int f0 = fb * C::feat_block;
             const uint32_t t_acc = tmem_base + acc * C::acc_cols + lane_addr;
             if constexpr (!C::swap) {
@@ -497,7 +506,7 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     }
     pdl_wait();  // the offsets (and the token rows) come from earlier kernels
     pdl_trigger();
-    build_prefix(p.offsets, p.N, kPairRows, p.rule, prefix, warp_sums);  // contains __syncthreads
+    build_prefix(p.offsets, p.N, p.rows, kPairRows, p.rule, prefix, warp_sums);  // contains __syncthreads
     tc_fence_before();
     cluster_sync();  // both CTAs' barriers are initialised and their TMEM allocated
     tc_fence_after();
@@ -518,7 +527,9 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             for (int tile = cid; tile < total_tiles && ok; tile += ncl) {
                 int e, pb, fb;
                 tile_coords(tile, nfb, prefix, p.N, e, pb, fb);
-                const int rows0 = p.offsets[e] + pb * kPairRows + (int)rank * kBM;
+                int seg0, cnt;
+                expert_segment(p.offsets, e, p.rows, seg0, cnt);
+                const int rows0 = seg0 + pb * kPairRows + (int)rank * kBM;
                 const int f0 = fb * feat_block + (GLU ? 0 : (int)rank * kBM);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % kPairStages;
@@ -585,10 +596,11 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             tc_fence_after();
             int e, pb, fb;
             tile_coords(tile, nfb, prefix, p.N, e, pb, fb);
-            const int cnt = p.offsets[e + 1] - p.offsets[e];
+            int seg0, cnt;
+            expert_segment(p.offsets, e, p.rows, seg0, cnt);
             const int r = (int)rank * kBM + q * 32 + lane;       // row inside the 256-row pair tile
             const bool row_ok = r < cnt - pb * kPairRows;
-            __nv_bfloat16 *orow = p.out + (int64_t)(p.offsets[e] + pb * kPairRows + r) * p.out_dim;
+            __nv_bfloat16 *orow = p.out + (int64_t)(seg0 + pb * kPairRows + r) * p.out_dim;
             const int f0 = fb * feat_block;
             const uint32_t t_acc = tmem_base + acc * 256 + lane_addr;
             constexpr int chunks = GLU ? 4 : 8;
@@ -729,13 +741,13 @@ cudaError_t launch_swap(const void *act, const int32_t *row_token, const int32_t
         !make_map_3d(&mdn, wd, N, d, I, kBM))
         return cudaErrorInvalidValue;
     const int64_t tok_blocks = cdiv(P, BNT) + N;
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token, kBlocksAll};
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token, kBlocksAll, (int)P};
     cudaError_t err = row_token
         ? launch_mode<SWAP_GLU, BNT, true>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s)
         : launch_mode<SWAP_GLU, BNT, false>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s);
     if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
-    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksAll};
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksAll, (int)P};
     return launch_mode<SWAP_PLAIN, BNT, false>(mh, mdn, mdn, p2, tok_blocks * cdiv(d, 128), s);
 }
 
@@ -785,14 +797,15 @@ cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32
     // 256-row pair tiles for every full block and every last block of more than 128 rows, then
     // single-CTA 128-row tiles for the last blocks of at most 128 rows (no MMA on 128 padding rows)
     const int64_t pair_blocks = cdiv(P, kPairRows) + N;  // bound of sum_e ceil(count_e / 256)
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, nullptr, kBlocksPairMain};
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, nullptr, kBlocksPairMain, (int)P};
     cudaError_t err = launch_pair<true>(mx, mg, mu, p1, pair_blocks * cdiv(I, 128), s);
     if (err != cudaSuccess) return err;
     p1.rule = kBlocksSmallRest;
     err = launch_mode<NORMAL_GLU, 0, false>(mx, mg, mu, p1, N * cdiv(I, 128), s);
     if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
-    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksPairMain};
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksPairMain,
+              (int)P};
     err = launch_pair<false>(mh, mdn, mdn, p2, pair_blocks * cdiv(d, 256), s);
     if (err != cudaSuccess) return err;
     // the single-CTA down tiles load all 256 W_down rows of their feature block in one box

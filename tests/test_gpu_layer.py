@@ -190,6 +190,58 @@ def test_expert_ffn_standalone_few_tokens(T):
     assert max_rel_err(host(y_perm), rows_ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("T,dtype", [(5, "bf16"), (333, "bf16"), (2000, "bf16"), (64, "f32")])
+def test_expert_ffn_clamps_offsets_to_the_rows(T, dtype):
+    """Offsets that no permutation wrote -- a negative start, an empty expert, an end past P -- are
+    clamped to [0, P): every row keeps the FFN of the expert whose clamped segment holds it, and
+    no row outside y_perm is written (guard rows on both sides, wider than the overshoot, so an
+    unclamped store would land in them)."""
+    w = WORKLOADS["decode_t32"].with_(T=T, d=256, I=192, dtype=dtype)
+    inp = synth.layer_inputs(w, seed=50 + T)
+    P, N = w.P, w.N
+    rng = np.random.default_rng(T)
+    cuts = np.sort(rng.choice(np.arange(1, P), N - 1, replace=False)).astype(np.int32)
+    offsets = np.concatenate([[-7], cuts, [P + 300]]).astype(np.int32)
+    offsets[5] = offsets[4]                                   # expert 4 empty
+    begin = np.clip(offsets[:-1], 0, P)
+    end = np.clip(np.maximum(offsets[1:], begin), 0, P)
+    experts = np.repeat(np.arange(N, dtype=np.int32), end - begin)
+    assert len(experts) == P
+    tokens = rng.integers(0, T, size=P).astype(np.int32)
+    c = config(w)
+    ws = moge.alloc_workspace(c)
+    d_inp = upload_layer(inp)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    guard = 512
+    buf = torch.full((P + 2 * guard, w.d), 5.0, dtype=tdt, device=DEV)
+    moge.moge_expert_ffn(c, dev(inp["x"][tokens]), dev(offsets), d_inp["w_gate"], d_inp["w_up"],
+                         d_inp["w_down"], buf[guard:guard + P], ws)
+    torch.cuda.synchronize()
+    got = host(buf)
+    sentinel = host(torch.full((1, w.d), 5.0, dtype=tdt))[0]
+    assert np.all(got[:guard] == sentinel) and np.all(got[guard + P:] == sentinel)
+    rows_ref = oracle.expert_ffn_pairs(tokens, experts, inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
+    assert max_rel_err(got[guard:guard + P], rows_ref) <= TOL[dtype]
+
+
+def test_combine_treats_out_of_range_rows_as_absent():
+    """pair_row entries outside [0, T*K) (-1 from a skipped expert id, or past the last row) add
+    nothing to the token's output."""
+    w = WORKLOADS["decode_t32"].with_(T=200, d=256, I=64)
+    rng = np.random.default_rng(3)
+    yp = synth.normal(8, synth.TID_X, (w.P, w.d), 1.0, "bf16")
+    pair_row = rng.permutation(w.P).astype(np.int32).reshape(w.T, w.K)
+    gate = rng.random((w.T, w.K)).astype(np.float32)
+    absent = rng.random(pair_row.shape) < 0.15
+    pair_row[absent] = np.resize(np.array([-1, w.P, w.P + 7, 1 << 30], dtype=np.int32), int(absent.sum()))
+    c = config(w)
+    y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=DEV)
+    moge.moge_combine(c, dev(yp), dev(pair_row), dev(gate), y)
+    torch.cuda.synchronize()
+    y_ref = oracle.combine_rows(yp, np.where(absent, 0, pair_row), np.where(absent, 0.0, gate.astype(np.float64)))
+    assert np.max(np.abs(as_f64(host(y)) - y_ref) / (np.abs(y_ref) + 1e-3)) < 2 ** -7
+
+
 def test_layer_with_1024_experts():
     """The largest expert count the library takes (N=1024; scores on CUDA cores for N > 256)."""
     w = WORKLOADS["decode_t32"].with_(name="n1024", T=300, d=256, N=1024, M=8, kpg=1, I=128)
