@@ -282,6 +282,34 @@ def stage_breakdown(layer, steps):
             for s, name in enumerate(moge.STAGE_NAMES)}
 
 
+def graph_steps(layer, steps, dist):
+    """The same step captured once into a CUDA graph and replayed `steps` times: no host work per
+    step (no argument checks, tensor-map encoding or launch calls).  ms per step from CUDA events
+    around the replays, max over ranks."""
+    import torch
+    layer.moge.moge_set_stage_events(None)
+    layer.step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.step()
+    for _ in range(3):
+        g.replay()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(steps):
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    if layer.moge.moge_query_device_status(layer.ws) != 0:
+        raise RuntimeError("device status word set during the graph replays")
+    del g
+    return max_over_ranks(start.elapsed_time(end) / steps, dist, layer.dev)
+
+
 def e2e_steps(layer, steps, dist):
     """Same metric through the public call with host buffers.  Every step copies its input x from
     pinned host memory to the device and its output y back to pinned host memory.  The copies run
@@ -456,6 +484,11 @@ def run_ours(args):
         ms, gate_up_ms, launches = timed_steps(prefill, args.steps, args.warmup, dist, clock=clk)
     clocks = clk.summary()
     stages = stage_breakdown(prefill, min(args.steps, 50))
+    graph = None
+    if args.graph_steps > 0:
+        gms = graph_steps(prefill, args.graph_steps, dist)
+        graph = {"value": round(job_tokens_per_s(wp.T, ws_n, gms), 1), "unit": "tokens/s",
+                 "ms_per_step": round(gms, 4), "steps": args.graph_steps}
     counts = prefill.aux["counts"].cpu().numpy()
     score = float(prefill.aux["score"][0].item())
 
@@ -465,12 +498,17 @@ def run_ours(args):
         dec = Layer(wd, d_inp, device)
         dms, dgate_up_ms, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist)
         dstages = stage_breakdown(dec, min(args.decode_steps, 100))
+        dgraph = None
+        if args.graph_steps > 0:
+            dgms = graph_steps(dec, 3 * args.graph_steps, dist)
+            dgraph = {"value": round(job_tokens_per_s(wd.T, ws_n, dgms), 1), "unit": "tokens/s",
+                      "ms_per_step": round(dgms, 4), "steps": 3 * args.graph_steps}
         dcounts = dec.aux["counts"].cpu().numpy()
         decode = {"workload": wd.name, "value": round(job_tokens_per_s(wd.T, ws_n, dms), 1), "unit": "tokens/s",
                   "ms_per_step": round(dms, 4), "steps": args.decode_steps,
                   "roofline": gate_up_roofline(wd, dcounts, dgate_up_ms, pk, peak_kind),
                   "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
-                  "stage_ms": dstages, "gpu_launches": int(dlaunches)}
+                  "stage_ms": dstages, "cuda_graph": dgraph, "gpu_launches": int(dlaunches)}
 
     # the same layers with Pangu Pro's 4 shared experts added (every token visits each of them)
     shared = None
@@ -538,6 +576,7 @@ def run_ours(args):
         "roofline": gate_up_roofline(wp, counts, gate_up_ms, pk, peak_kind),
         "layer_roofline": layer_roofline(wp, counts, ms, pk),
         "stage_ms": stages,
+        "cuda_graph": graph,
         "imbalance_score": score,
         "clocks": clocks,
         "e2e": e2e,
@@ -653,6 +692,8 @@ def main():
     ap.add_argument("--workload", default="prefill_t8192", choices=["prefill_t8192"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
     ap.add_argument("--shared-steps", type=int, default=50, help="steps of the shared-expert layers (0: skip)")
+    ap.add_argument("--graph-steps", type=int, default=100,
+                    help="replays of the step captured as a CUDA graph (decode: 3x; 0: skip)")
     ap.add_argument("--study-batches", type=int, default=1000, help="Monte-Carlo study batches (0: skip)")
     ap.add_argument("--pangu-steps", type=int, default=30, help="steps at Pangu Pro dims, K'=1 (0: skip)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -4,6 +4,8 @@
 #include <stdlib.h>
 
 #include <atomic>
+#include <map>
+#include <mutex>
 
 #include "common.cuh"
 #include "ffn_tc.cuh"
@@ -17,6 +19,21 @@ thread_local void *const *t_stage_events = nullptr;
 
 namespace moge {
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+cudaError_t set_max_smem_impl(const void *kernel, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, size_t> done;  // (kernel, device) -> bytes set
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(kernel, dev);
+    const auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err == cudaSuccess) done[key] = bytes;
+    return err;
+}
 void mark_stage(int stage, cudaStream_t s) {
     if (t_stage_events && stage >= 0 && stage <= MOGE_NUM_STAGES && t_stage_events[stage])
         cudaEventRecord((cudaEvent_t)t_stage_events[stage], s);

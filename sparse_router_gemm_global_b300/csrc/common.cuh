@@ -165,6 +165,14 @@ inline WsLayout ws_layout(const moge_config_t &c, int64_t S = 0) {
     return L;
 }
 
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per (kernel, device) and
+// size: the largest size set so far is remembered, so steady-state launches (and launches
+// inside a CUDA graph capture) make no attribute call.  Defined in api.cu.
+cudaError_t set_max_smem_impl(const void *kernel, size_t bytes);
+template <typename Kernel> cudaError_t set_max_smem(Kernel kernel, size_t bytes) {
+    return set_max_smem_impl(reinterpret_cast<const void *>(kernel), bytes);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Launchers (defined in the .cu files).  All return cudaGetLastError() after launching.
 // ---------------------------------------------------------------------------------------------

@@ -702,7 +702,7 @@ cudaError_t launch_mode(const CUtensorMap &ma, const CUtensorMap &mb0, const CUt
                         int64_t tile_bound, cudaStream_t s) {
     using C = Cfg<MODE, BNT>;
     auto kern = ffn_tc_kernel<MODE, BNT, GATHER>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes);
+    cudaError_t err = set_max_smem(kern, (int)C::smem_bytes);
     if (err != cudaSuccess) return err;
     const int grid = (int)std::min<int64_t>(tile_bound, (int64_t)sm_count());
     if (grid <= 0) return cudaSuccess;
@@ -715,7 +715,7 @@ template <bool GLU>
 cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1, const Params &p,
                         int64_t pair_tile_bound, cudaStream_t s) {
     auto kern = ffn_tc_pair_kernel<GLU>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem);
+    cudaError_t err = set_max_smem(kern, (int)kPairSmem);
     if (err != cudaSuccess) return err;
     const int grid = (int)std::min<int64_t>(2 * pair_tile_bound, (int64_t)(sm_count() & ~1));  // whole pairs
     if (grid <= 0) return cudaSuccess;

@@ -129,8 +129,7 @@ cudaError_t launch_imbalance_study(int64_t T, int64_t N, int64_t M, int64_t kpg,
     count_launches(1);
     if (T > 0) {
         const size_t smem = imbalance_study_smem_bytes(N, M);
-        cudaError_t err = cudaFuncSetAttribute(study_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
+        cudaError_t err = set_max_smem(study_route_kernel, (int)smem);
         if (err != cudaSuccess) return err;
         const uint64_t key = mix64(seed ^ kStudyTensorId);
         constexpr int64_t kMaxGridY = 65535;

@@ -107,8 +107,7 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
     const size_t smem_scatter = (size_t)permute_block_smem_words((int)N, (int)M) * 4;
     cudaError_t err;
     if (T <= kChunk) {
-        err = cudaFuncSetAttribute(permute_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_scatter);
+        err = set_max_smem(permute_single_kernel, (int)smem_scatter);
         if (err != cudaSuccess) return err;
         err = launch_pdl(permute_single_kernel, dim3(1), dim3(kChunk), smem_scatter, s, idx, T, (int)K, (int)N,
                          counts, offsets, pair_row, row_token, status, (int)M, group_load, score);
@@ -117,11 +116,9 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
     }
     const int chunks = (int)cdiv(T, kChunk);
     const size_t smem_count = (size_t)kWarps * N * 4;
-    err = cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_count);
+    err = set_max_smem(permute_count_kernel, (int)smem_count);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_scatter);
+    err = set_max_smem(permute_scatter_kernel, (int)smem_scatter);
     if (err != cudaSuccess) return err;
     err = launch_pdl(permute_count_kernel, dim3(chunks), dim3(kChunk), smem_count, s, idx, T, (int)K, (int)N,
                      chunk_counts, status);

@@ -39,8 +39,7 @@ cudaError_t launch_route_select(const float *logits, int64_t T, int64_t N, int64
     if (T == 0) return cudaSuccess;
     const int rows_pb = N <= 639 ? kSelectRows : kSelectRows / 2;
     const size_t smem = (size_t)rows_pb * (N + 1) * sizeof(float);
-    cudaError_t err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
+    cudaError_t err = set_max_smem(route_select_kernel, (int)smem);
     if (err != cudaSuccess) return err;
     const int groups = global ? 1 : (int)M;
     const int G = global ? (int)N : (int)(N / M);

@@ -209,13 +209,11 @@ cudaError_t launch_route_small(const void *x, const void *w_r, const float *bias
     const dim3 grid((unsigned)cdiv(T, kTokTile), (unsigned)cdiv(N, kExpTile));
     cudaError_t err;
     if (dtype == MOGE_BF16) {
-        err = cudaFuncSetAttribute(route_small_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem);
+        err = set_max_smem(route_small_kernel<__nv_bfloat16>, (int)smem);
         if (err != cudaSuccess) return err;
         err = launch_pdl(route_small_kernel<__nv_bfloat16>, grid, dim3(kThreads), smem, s, p);
     } else {
-        err = cudaFuncSetAttribute(route_small_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem);
+        err = set_max_smem(route_small_kernel<float>, (int)smem);
         if (err != cudaSuccess) return err;
         err = launch_pdl(route_small_kernel<float>, grid, dim3(kThreads), smem, s, p);
     }

@@ -241,7 +241,7 @@ cudaError_t launch_router_tc(const void *x, const void *w_r, const float *bias, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = set_max_smem(router_tc_kernel, (int)smem);
     if (err != cudaSuccess) return err;
     // the slices of a tile form one cluster (1 x kslices)
     cudaLaunchConfig_t cfg{};
