@@ -53,7 +53,9 @@ def call(c, S, d, out, ws):
 
 
 def snapshot(out):
-    return {k: host(v) for k, v in out.items()}
+    res = {k: host(v) for k, v in out.items()}
+    res["score"] = res["score"][:1]  # one float; the buffer is padded to 16 bytes
+    return res
 
 
 @pytest.mark.parametrize("case", list(CASES))
