@@ -113,12 +113,13 @@ static_assert(kSmallRouteMaxT <= kPermuteChunk, "the small router permutes its t
 
 // Tile plan of the bf16 grouped GEMM for `rows` (token, expert) rows over `experts` experts of a
 // batch of T tokens.  Weights-as-M tiles stream each expert's weights at full MMA height with
-// the expert's token rows as the MMA's N (16/32/64 per tile, several tiles for a larger
+// the expert's token rows as the MMA's N (16/32/64/128 per tile, several tiles for a larger
 // expert); they suit batches whose experts hold few rows, where 256-row tokens-as-M tiles would
 // be mostly padding.  With at most 32 tokens the GEMM gathers the token rows from x itself
 // (TMA gather4, at most 8 copies per k-block); otherwise the rows are first copied to x_perm.
-enum FfnTiles { kTilesSwap16 = 16, kTilesSwap32 = 32, kTilesSwap64 = 64, kTilesPair = 256 };
-constexpr int64_t kSwapMaxMeanRows = 96;  // weights-as-M tiles while rows / experts <= this
+enum FfnTiles { kTilesSwap16 = 16, kTilesSwap32 = 32, kTilesSwap64 = 64, kTilesSwap128 = 128, kTilesPair = 256 };
+constexpr int64_t kSwap64MaxMeanRows = 48;  // 64-token weights-as-M tiles while rows / experts <= this
+constexpr int64_t kSwapMaxMeanRows = 104;   // 128-token weights-as-M tiles while rows / experts <= this
 struct FfnPlan {
     int tiles;
     bool gather_in_gemm;
@@ -126,7 +127,8 @@ struct FfnPlan {
 inline FfnPlan ffn_plan(int64_t T, int64_t rows, int64_t experts) {
     if (T <= 16) return {kTilesSwap16, true};
     if (T <= 32) return {kTilesSwap32, true};
-    if (rows <= kSwapMaxMeanRows * experts) return {kTilesSwap64, false};
+    if (rows <= kSwap64MaxMeanRows * experts) return {kTilesSwap64, false};
+    if (rows <= kSwapMaxMeanRows * experts) return {kTilesSwap128, false};
     return {kTilesPair, false};
 }
 

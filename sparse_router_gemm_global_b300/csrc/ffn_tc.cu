@@ -784,6 +784,9 @@ cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32
         case kTilesSwap64:
             return launch_swap<64>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status,
                                    s);
+        case kTilesSwap128:
+            return launch_swap<128>(act, row_token, offsets, N, P, T, d, I, w_gate, w_up, w_down, h, y_perm, status,
+                                    s);
         default:
             break;
     }

@@ -150,12 +150,13 @@ def test_stress_n256_sampled():
     check_layer(w, inp, got, tokens=toks)
 
 
-@pytest.mark.parametrize("T", [16, 17, 32, 33, 64, 65, 128, 256, 257, 384, 385])
+@pytest.mark.parametrize("T", [16, 17, 32, 33, 64, 65, 128, 192, 193, 256, 257, 384, 416, 417])
 def test_bf16_layer_at_path_boundaries(T):
-    """Token counts on both sides of every switch: weights-as-M tile widths 16/32/64 and the
-    in-GEMM row gather (T <= 32), the small router (64/65), several 64-token blocks per expert
-    (128, 256), one vs several permutation chunks (256/257), weights-as-M -> tokens-as-M tiles
-    (384/385: 96 rows per expert on average with K=16 of N=64)."""
+    """Token counts on both sides of every switch (K=16 of N=64 experts: T/4 rows per expert on
+    average): weights-as-M tile widths 16/32 and the in-GEMM row gather (T <= 32), the small
+    router (64/65), 64-token tiles -> 128-token tiles (192/193: 48 rows per expert), one vs several
+    permutation chunks (256/257), several 128-token blocks per expert (384), weights-as-M ->
+    tokens-as-M tiles (416/417: 104 rows per expert)."""
     w = WORKLOADS["decode_t32"].with_(name=f"edge_{T}", T=T, d=384, I=192)
     inp = synth.layer_inputs(w, seed=100 + T)
     got = run_layer(w, upload_layer(inp))
