@@ -214,19 +214,39 @@ class Layer:
 
 
 EVENT_STRIDE = 10  # the gate/up GEMM is timed on every 10th step of the timed region
+# Minimum warm-up time before each timed region (on top of --warmup steps).  Measured on a B300:
+# from idle, 5 warm-up steps left the prefill step 0.8 % faster than its steady state (4.28 vs
+# 4.32 ms); right after the prefill, the decode step needs ~100 steps (30 ms) to recover from
+# 0.337 to 0.317 ms.
+WARM_S = {"prefill": 0.5, "decode": 0.2}
 
 
-def timed_steps(layer, steps, warmup, dist, clock=None):
-    """K steps bracketed by barrier + synchronize.  Inside the timed region the library records
-    the two events around the grouped gate/up GEMM (the roofline kernel), on its own stream, on
-    every EVENT_STRIDE-th step: each recorded event costs the step a few microseconds, so the
-    step time carries almost none of that instrumentation while the GEMM is still timed live.
-    Returns (ms/step max over ranks, gate/up ms per launch, kernel launches in the region)."""
+def warm_up(layer, steps, min_seconds):
+    """At least `steps` steps and at least `min_seconds` of them: under the power cap the SM clock
+    takes tens of milliseconds to settle after a change of load (up from idle, or down to a
+    lighter layer after a heavy one), and the timed region should see the layer's own steady
+    state, not the previous one."""
     import torch
-    moge = layer.moge
-    for _ in range(warmup):
+    t0 = time.perf_counter()
+    for _ in range(steps):
         layer.step()
     torch.cuda.synchronize()
+    while time.perf_counter() - t0 < min_seconds:
+        for _ in range(10):
+            layer.step()
+        torch.cuda.synchronize()
+
+
+def timed_steps(layer, steps, warmup, dist, clock=None, min_warm_s=0.0):
+    """K steps bracketed by barrier + synchronize, after warm_up(warmup, min_warm_s).  Inside the
+    timed region the library records the two events around the grouped gate/up GEMM (the roofline
+    kernel), on its own stream, on every EVENT_STRIDE-th step: each recorded event costs the step a
+    few microseconds, so the step time carries almost none of that instrumentation while the GEMM
+    is still timed live.  Returns (ms/step max over ranks, gate/up ms per launch, kernel launches
+    in the region)."""
+    import torch
+    moge = layer.moge
+    warm_up(layer, warmup, min_warm_s)
     gu, dn = moge.STAGE_NAMES.index("gate_up"), moge.STAGE_NAMES.index("down")
     evs = []
     for i in range(steps):
@@ -282,10 +302,11 @@ def stage_breakdown(layer, steps):
             for s, name in enumerate(moge.STAGE_NAMES)}
 
 
-def graph_steps(layer, steps, dist):
+def graph_steps(layer, steps, dist, min_warm_s=0.0):
     """The same step captured once into a CUDA graph and replayed `steps` times: no host work per
-    step (no argument checks, tensor-map encoding or launch calls).  ms per step from CUDA events
-    around the replays, max over ranks."""
+    step (no argument checks, tensor-map encoding or launch calls).  Warm-up: at least 3 replays
+    and min_warm_s seconds of them.  ms per step from CUDA events around the replays, max over
+    ranks."""
     import torch
     layer.moge.moge_set_stage_events(None)
     layer.step()
@@ -293,8 +314,14 @@ def graph_steps(layer, steps, dist):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         layer.step()
+    t0 = time.perf_counter()
     for _ in range(3):
         g.replay()
+    torch.cuda.synchronize()
+    while time.perf_counter() - t0 < min_warm_s:
+        for _ in range(10):
+            g.replay()
+        torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         torch.distributed.barrier()
@@ -349,8 +376,12 @@ def e2e_steps(layer, steps, dist):
         for b in range(nb):
             comp.wait_event(ev_out[b])
 
-    run(2)
+    t0 = time.perf_counter()  # warm-up: at least 3 steps and WARM_S["prefill"] seconds
+    run(3)
     torch.cuda.synchronize()
+    while time.perf_counter() - t0 < WARM_S["prefill"]:
+        run(10)
+        torch.cuda.synchronize()
     if dist:
         torch.distributed.barrier()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -481,7 +512,8 @@ def run_ours(args):
         os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
     gpu_index = int(phys) if phys.isdigit() else local
     with ClockSampler(gpu_index) as clk:
-        ms, gate_up_ms, launches = timed_steps(prefill, args.steps, args.warmup, dist, clock=clk)
+        ms, gate_up_ms, launches = timed_steps(prefill, args.steps, args.warmup, dist, clock=clk,
+                                               min_warm_s=WARM_S["prefill"])
     clocks = clk.summary()
     stages = stage_breakdown(prefill, min(args.steps, 50))
     counts = prefill.aux["counts"].cpu().numpy()
@@ -491,11 +523,12 @@ def run_ours(args):
     decode = None
     if args.decode_steps > 0:
         dec = Layer(wd, d_inp, device)
-        dms, dgate_up_ms, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist)
+        dms, dgate_up_ms, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist,
+                                                  min_warm_s=WARM_S["decode"])
         dstages = stage_breakdown(dec, min(args.decode_steps, 100))
         dgraph = None
         if args.graph_steps > 0:
-            dgms = graph_steps(dec, 3 * args.graph_steps, dist)
+            dgms = graph_steps(dec, 3 * args.graph_steps, dist, min_warm_s=WARM_S["decode"])
             dgraph = {"value": round(job_tokens_per_s(wd.T, ws_n, dgms), 1), "unit": "tokens/s",
                       "ms_per_step": round(dgms, 4), "steps": 3 * args.graph_steps}
         dcounts = dec.aux["counts"].cpu().numpy()
@@ -509,7 +542,7 @@ def run_ours(args):
     # seconds-long load that would leave the short decode window starting power-throttled)
     graph = None
     if args.graph_steps > 0:
-        gms = graph_steps(prefill, args.graph_steps, dist)
+        gms = graph_steps(prefill, args.graph_steps, dist, min_warm_s=WARM_S["prefill"])
         graph = {"value": round(job_tokens_per_s(wp.T, ws_n, gms), 1), "unit": "tokens/s",
                  "ms_per_step": round(gms, 4), "steps": args.graph_steps}
 
@@ -519,7 +552,7 @@ def run_ours(args):
         shared = {"n_shared": SHARED_EXPERTS}
         for name, w, n in (("prefill", wp, args.shared_steps), ("decode", wd, 3 * args.shared_steps)):
             L = Layer(w, d_inp, device, n_shared=SHARED_EXPERTS)
-            sms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist)
+            sms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist, min_warm_s=WARM_S[name])
             rows = w.P + SHARED_EXPERTS * w.T
             shared[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "value": round(job_tokens_per_s(w.T, ws_n, sms), 1),
                             "unit": "tokens/s", "ms_per_step": round(sms, 4), "steps": n,
@@ -534,7 +567,7 @@ def run_ours(args):
         p_inp = upload(synth.layer_inputs(wpp, seed=DEFAULT_SEED, n_shared=SHARED_EXPERTS), device)
         for name, w, n in (("prefill", wpp, args.pangu_steps), ("decode", wpd, 3 * args.pangu_steps)):
             L = Layer(w, p_inp, device, n_shared=SHARED_EXPERTS)
-            pms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist)
+            pms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist, min_warm_s=WARM_S[name])
             rows = w.P + SHARED_EXPERTS * w.T
             touched = int((L.aux["counts"].cpu().numpy() > 0).sum()) + SHARED_EXPERTS
             pangu[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "d": w.d, "I": w.I, "K": w.K,
@@ -566,6 +599,7 @@ def run_ours(args):
         "n_gpus": ws_n,
         "steps": args.steps,
         "warmup": args.warmup,
+        "warmup_min_seconds": WARM_S,
         "ms_per_step": round(ms, 4),
         "higher_is_better": True,
         "scaling": "weak",
