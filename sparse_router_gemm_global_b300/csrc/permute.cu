@@ -1,5 +1,6 @@
 // Permutation of (token, slot) pairs into expert-contiguous rows:
-// histogram -> prefix sum -> deterministic scatter, then the row gather.
+// histogram -> prefix sum -> deterministic scatter, then the row copy into x_perm (token-major
+// from pair_row, or row-major through row_token when the caller wants no pair_row).
 // Tokens are cut into chunks of kPermuteChunk (one block each, one token per thread); the
 // block-level steps are in permute_block.cuh.
 #include <algorithm>
@@ -135,12 +136,13 @@ cudaError_t launch_permute(const int32_t *idx, int64_t T, int64_t K, int64_t N, 
 }
 
 // ---------------------------------------------------------------------------------------------
-// Row gather x_perm[r,:] = x[row_token[r],:]; one warp per row, 16-byte vectors, each lane
-// issuing 8 loads before their stores so that a row's reads are in flight together.
-// Only rows r < offsets[N] (the pairs that exist) are copied.  Every row of x is read once per
-// expert its token selected, so x is loaded with an evict-last L2 policy and x_perm (written
-// once, read back much later) is stored with the streaming hint: the copy then moves about one
-// pass of x_perm through HBM instead of also re-reading x.
+// Row gather x_perm[r,:] = x[row_token[r],:] (moge_permute without pair_row); one warp per row,
+// 16-byte vectors, each lane issuing 8 loads before their stores so that a row's reads are in
+// flight together.  Only rows r < offsets[N] (the pairs that exist) are copied.  Every row of x
+// is read once per expert its token selected, so x is loaded with an evict-last L2 policy and
+// x_perm (written once, read back much later) is stored with the streaming hint; still, at the
+// prefill shape it moved 1.51 GB against 1.14 GB algorithmic, where the token-major copy below
+// moves 1.08 GB.
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ int4 ld_keep(const int4 *p, uint64_t pol) {
     int4 v;
