@@ -213,6 +213,23 @@ def shared_experts_tokens(tokens, n_routed: int, n_shared: int, x, w_gate, w_up,
     return out
 
 
+def values64(a) -> np.ndarray:
+    """An fp32 or raw-bf16 (uint16) array as exact float64 values (bf16 bits b are the fp32 with
+    bits b << 16)."""
+    if a.dtype == np.uint16:
+        return (np.ascontiguousarray(a).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if a.dtype == np.float32:
+        return a.astype(np.float64)
+    raise TypeError(f"oracle takes fp32 or raw-bf16 (uint16) arrays, got {a.dtype}")
+
+
+def residual_tokens(tokens, residual) -> np.ndarray:
+    """[n, d] float64: the residual-stream rows of the listed tokens.  The pages describe no
+    residual; the reading taken is the transformer block's: the layer's output is added once per
+    token to the residual stream r, y = r + sum_k gate_k FFN_k(x) + sum_s FFN_s(x), unweighted."""
+    return values64(residual)[_c(tokens, np.int32)]
+
+
 def combine_rows(rows, pair_row, gate64) -> np.ndarray:
     """y [T, d] float64 = sum_k gate[t,k] * rows[pair_row[t,k]] (the combine step alone)."""
     dt = _dt(rows)
@@ -243,7 +260,7 @@ def route(logits, M: int, kpg: int, mode: str = "grouped") -> dict:
 
 
 def layer_forward(x, w_router, bias, w_gate, w_up, w_down, M: int, kpg: int, tokens=None,
-                  logits=None, n_shared: int = 0) -> dict:
+                  logits=None, n_shared: int = 0, residual=None) -> dict:
     """The whole MoGE layer for the listed tokens (all tokens if None).
 
     Routing is computed for every token (the permutation and the loads need
@@ -251,7 +268,8 @@ def layer_forward(x, w_router, bias, w_gate, w_up, w_down, M: int, kpg: int, tok
     ``logits`` replaces the router projection by those scores (used to
     re-run the FFN under another routing).  With ``n_shared`` > 0 the weight
     arrays hold N + n_shared experts and the shared experts' outputs are added
-    (see shared_experts_tokens).
+    (see shared_experts_tokens); with ``residual`` [T, d] its rows are added too
+    (see residual_tokens).
     """
     if logits is None:
         logits = router_logits(x, w_router, bias)
@@ -263,4 +281,6 @@ def layer_forward(x, w_router, bias, w_gate, w_up, w_down, M: int, kpg: int, tok
     r["y"] = combine_tokens(r["tokens"], r["idx"], r["gate64"], x, w_gate, w_up, w_down)
     if n_shared:
         r["y"] = r["y"] + shared_experts_tokens(r["tokens"], w_router.shape[0], n_shared, x, w_gate, w_up, w_down)
+    if residual is not None:
+        r["y"] = r["y"] + residual_tokens(r["tokens"], residual)
     return r
