@@ -230,6 +230,22 @@ moge_status_t moge_layer_forward_shared(const moge_config_t *cfg, int64_t n_shar
                                         const void *w_up, const void *w_down, void *y, const moge_aux_t *aux,
                                         void *ws, size_t ws_bytes, moge_stream_t stream);
 
+/* The layer (with S = n_shared >= 0 shared experts, as moge_layer_forward_shared)
+ * added to a residual stream: the pages describe no residual; the reading taken
+ * is the transformer block's, where the layer's output is added once per token,
+ * unweighted, to the hidden state it was computed from:
+ *   y[t] = residual[t] + sum_k gate[t,k] FFN_{idx[t,k]}(x[t]) + sum_{s<S} FFN_{N+s}(x[t]),
+ * summed in fp32 (routed slots in slot order, then shared experts, then the
+ * residual) and rounded once.  residual [T,d] has the activation dtype, is
+ * 16-byte aligned and must not be NULL when T > 0; y may be the residual buffer
+ * itself (in-place update of the residual stream) or any other [T,d] buffer.
+ * Everything else (arguments, aux outputs, workspace size
+ * moge_workspace_bytes_shared(cfg, n_shared), errors) is moge_layer_forward_shared's. */
+moge_status_t moge_layer_forward_residual(const moge_config_t *cfg, int64_t n_shared, const void *x,
+                                          const void *residual, const void *w_router, const float *bias,
+                                          const void *w_gate, const void *w_up, const void *w_down, void *y,
+                                          const moge_aux_t *aux, void *ws, size_t ws_bytes, moge_stream_t stream);
+
 /* Monte-Carlo study of the imbalance score (Pangu Pro MoE explainer, section 1:
  * a Monte-Carlo simulation finds the imbalance score of conventional top-K
  * routing almost always above zero; MoGE's group top-K' keeps it at zero).

@@ -13,4 +13,5 @@ from .binding import (  # noqa: F401
     moge_imbalance_score, moge_layer_forward, moge_abi_version, moge_status_string, library_path, load,
     moge_set_stage_events, moge_kernel_launch_count, MOGE_NUM_STAGES, STAGE_NAMES, moge_permute_noalloc,
     moge_imbalance_study, moge_workspace_bytes_shared, moge_layer_forward_shared, moge_selftest_bounded_wait,
+    moge_layer_forward_residual,
 )

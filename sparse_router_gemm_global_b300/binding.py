@@ -78,12 +78,16 @@ def load():
         lib.moge_workspace_bytes_shared.argtypes = [cfgp, ctypes.c_int64]
         lib.moge_layer_forward_shared.argtypes = [cfgp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp,
                                                   ctypes.POINTER(Aux), vp, sz, vp]
+        lib.moge_layer_forward_residual.argtypes = [cfgp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                    ctypes.POINTER(Aux), vp, sz, vp]
         lib.moge_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint64, vp, vp]
         lib.moge_imbalance_study.argtypes = [cfgp, ctypes.c_int64, ctypes.c_uint64, vp, vp, vp, vp, vp, vp]
         lib.moge_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         lib.moge_kernel_launch_count.restype = ctypes.c_uint64
-        for fn in ("moge_selftest_bounded_wait", "moge_layer_forward_shared", "moge_imbalance_study", "moge_set_stage_events", "moge_reset_device_status", "moge_query_device_status", "moge_route", "moge_permute",
-                   "moge_expert_ffn", "moge_combine", "moge_imbalance_score", "moge_layer_forward"):
+        for fn in ("moge_selftest_bounded_wait", "moge_layer_forward_shared", "moge_layer_forward_residual",
+                   "moge_imbalance_study", "moge_set_stage_events", "moge_reset_device_status",
+                   "moge_query_device_status", "moge_route", "moge_permute", "moge_expert_ffn", "moge_combine",
+                   "moge_imbalance_score", "moge_layer_forward"):
             getattr(lib, fn).restype = i32
         _lib = lib
         return lib
@@ -241,6 +245,15 @@ def moge_layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, y, ws, aux:
     _check("moge_layer_forward", load().moge_layer_forward(
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(y),
         ctypes.byref(a), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moge_layer_forward_residual(cfg, n_shared, x, residual, w_router, bias, w_gate, w_up, w_down, y, ws,
+                                aux: dict | None = None, stream=None) -> None:
+    a = Aux(*[_ptr((aux or {}).get(k)) for k, _ in Aux._fields_])
+    _check("moge_layer_forward_residual", load().moge_layer_forward_residual(
+        ctypes.byref(cfg), int(n_shared), _ptr(x), _ptr(residual), _ptr(w_router), _ptr(bias), _ptr(w_gate),
+        _ptr(w_up), _ptr(w_down), _ptr(y), ctypes.byref(a), _ptr(ws), ws.numel() if ws is not None else 0,
+        _stream(stream)))
 
 
 def moge_layer_forward_shared(cfg, n_shared, x, w_router, bias, w_gate, w_up, w_down, y, ws,

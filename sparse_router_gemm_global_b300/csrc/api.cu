@@ -131,10 +131,12 @@ moge_status_t ffn_impl(const moge_config_t *c, const void *act, const int32_t *r
                                        y_perm, st));
 }
 
-// The whole layer with S >= 0 shared experts (weights of N + S experts; S = 0 is the MoGE layer).
-moge_status_t layer_impl(const moge_config_t *cfg, int64_t S, const void *x, const void *w_router,
-                         const float *bias, const void *w_gate, const void *w_up, const void *w_down, void *y,
-                         const moge_aux_t *aux, void *ws, size_t ws_bytes, moge_stream_t stream) {
+// The whole layer with S >= 0 shared experts (weights of N + S experts; S = 0 is the MoGE layer)
+// and an optional residual stream added to the output (residual == nullptr: none).
+moge_status_t layer_impl(const moge_config_t *cfg, int64_t S, const void *x, const void *residual,
+                         const void *w_router, const float *bias, const void *w_gate, const void *w_up,
+                         const void *w_down, void *y, const moge_aux_t *aux, void *ws, size_t ws_bytes,
+                         moge_stream_t stream) {
     moge_status_t s = check_layer(cfg);
     if (s != MOGE_OK) return s;
     if (S < 0 || S > kMaxShared) return MOGE_ERR_INVALID_ARGUMENT;
@@ -142,7 +144,7 @@ moge_status_t layer_impl(const moge_config_t *cfg, int64_t S, const void *x, con
     if (!w_router || !w_gate || !w_up || !w_down) return MOGE_ERR_INVALID_ARGUMENT;
     if (cfg->T > 0 && (!x || !y)) return MOGE_ERR_INVALID_ARGUMENT;  // an empty batch may pass NULL
     moge_aux_t a = aux ? *aux : moge_aux_t{};
-    for (const void *p : {x, w_router, (const void *)bias, w_gate, w_up, w_down, (const void *)y,
+    for (const void *p : {x, residual, w_router, (const void *)bias, w_gate, w_up, w_down, (const void *)y,
                           (const void *)a.logits, (const void *)a.topk_idx, (const void *)a.topk_gate,
                           (const void *)a.counts, (const void *)a.offsets, (const void *)a.group_load,
                           (const void *)a.score})
@@ -205,7 +207,7 @@ moge_status_t layer_impl(const moge_config_t *cfg, int64_t S, const void *x, con
                        : ffn_impl(cfg, x_perm, nullptr, offsets, w_gate, w_up, w_down, y_perm, ws, st, S);
     if (s != MOGE_OK) return s;
     mark_stage(MOGE_STAGE_COMBINE, st);
-    e = launch_combine(y_perm, pair_row, gate, cfg->T, K, cfg->d, cfg->act_dtype, y, st, S, P);
+    e = launch_combine(y_perm, pair_row, gate, cfg->T, K, cfg->d, cfg->act_dtype, y, st, S, P, residual);
     mark_stage(MOGE_STAGE_IMBALANCE, st);  // empty: computed with the permutation
     mark_stage(MOGE_NUM_STAGES, st);
     return cuda_status(e);
@@ -328,7 +330,7 @@ moge_status_t moge_imbalance_score(const moge_config_t *cfg, const int32_t *coun
 moge_status_t moge_layer_forward(const moge_config_t *cfg, const void *x, const void *w_router, const float *bias,
                                  const void *w_gate, const void *w_up, const void *w_down, void *y,
                                  const moge_aux_t *aux, void *ws, size_t ws_bytes, moge_stream_t stream) {
-    return layer_impl(cfg, 0, x, w_router, bias, w_gate, w_up, w_down, y, aux, ws, ws_bytes, stream);
+    return layer_impl(cfg, 0, x, nullptr, w_router, bias, w_gate, w_up, w_down, y, aux, ws, ws_bytes, stream);
 }
 
 size_t moge_workspace_bytes_shared(const moge_config_t *cfg, int64_t n_shared) {
@@ -343,7 +345,17 @@ moge_status_t moge_layer_forward_shared(const moge_config_t *cfg, int64_t n_shar
                                         const void *w_router, const float *bias, const void *w_gate,
                                         const void *w_up, const void *w_down, void *y, const moge_aux_t *aux,
                                         void *ws, size_t ws_bytes, moge_stream_t stream) {
-    return layer_impl(cfg, n_shared, x, w_router, bias, w_gate, w_up, w_down, y, aux, ws, ws_bytes, stream);
+    return layer_impl(cfg, n_shared, x, nullptr, w_router, bias, w_gate, w_up, w_down, y, aux, ws, ws_bytes,
+                      stream);
+}
+
+moge_status_t moge_layer_forward_residual(const moge_config_t *cfg, int64_t n_shared, const void *x,
+                                          const void *residual, const void *w_router, const float *bias,
+                                          const void *w_gate, const void *w_up, const void *w_down, void *y,
+                                          const moge_aux_t *aux, void *ws, size_t ws_bytes, moge_stream_t stream) {
+    if (!residual && cfg && cfg->T > 0) return MOGE_ERR_INVALID_ARGUMENT;
+    return layer_impl(cfg, n_shared, x, residual, w_router, bias, w_gate, w_up, w_down, y, aux, ws, ws_bytes,
+                      stream);
 }
 
 moge_status_t moge_imbalance_study(const moge_config_t *cfg, int64_t batches, uint64_t seed, const float *bias,

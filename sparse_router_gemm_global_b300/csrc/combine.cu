@@ -1,6 +1,8 @@
 // Weighted combine: y[t,:] = sum_{k=0..K-1} gate[t,k] * y_perm[pair_row[t,k],:], summed in
 // slot order with fp32 accumulation and rounded once to the activation dtype; with S shared
-// experts their rows y_perm[shared_base + s*T + t,:] follow with weight 1, in order s = 0..S-1.
+// experts their rows y_perm[shared_base + s*T + t,:] follow with weight 1, in order s = 0..S-1,
+// and with a residual stream r the row r[t,:] is added last.  y may be r (each element is read
+// and then written by the same thread).
 // A pair_row entry outside [0, rows) (-1: the permutation skipped the slot's expert id) counts
 // as an absent slot.
 // Grid (token, column block): each thread owns one 16-byte column vector of one token and
@@ -16,7 +18,7 @@ constexpr int kSlotBatch = 8;
 template <typename T, int V>  // V elements per 16-byte vector
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_row, const float *__restrict__ gate,
-               int K, int64_t d, T *__restrict__ y, int S, int64_t shared_base, int64_t Tn, int64_t rows) {
+               int K, int64_t d, T *y, int S, int64_t shared_base, int64_t Tn, int64_t rows, const T *residual) {
     pdl_wait();
     pdl_trigger();
     const int64_t t = blockIdx.x;
@@ -62,6 +64,12 @@ combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_ro
             for (int i = 0; i < V; ++i) acc[i] += to_f32(e[i]);
         }
     }
+    if (residual) {
+        const int4 rv = reinterpret_cast<const int4 *>(residual + t * d)[v];
+        const T *e = reinterpret_cast<const T *>(&rv);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += to_f32(e[i]);
+    }
     int4 out;
     T *o = reinterpret_cast<T *>(&out);
 #pragma unroll
@@ -70,7 +78,8 @@ combine_kernel(const T *__restrict__ y_perm, const int32_t *__restrict__ pair_ro
 }
 
 cudaError_t launch_combine(const void *y_perm, const int32_t *pair_row, const float *gate, int64_t T,
-                           int64_t K, int64_t d, int dtype, void *y, cudaStream_t s, int64_t S, int64_t shared_base) {
+                           int64_t K, int64_t d, int dtype, void *y, cudaStream_t s, int64_t S, int64_t shared_base,
+                           const void *residual) {
     if (T == 0) return cudaSuccess;
     const int V = dtype == MOGE_BF16 ? 8 : 4;
     dim3 grid((unsigned)T, (unsigned)cdiv(d / V, kCombineThreads));
@@ -78,9 +87,9 @@ cudaError_t launch_combine(const void *y_perm, const int32_t *pair_row, const fl
     cudaError_t err = dtype == MOGE_BF16
         ? launch_pdl(combine_kernel<__nv_bfloat16, 8>, grid, dim3(kCombineThreads), 0, s,
                      (const __nv_bfloat16 *)y_perm, pair_row, gate, (int)K, d, (__nv_bfloat16 *)y, (int)S,
-                     shared_base, T, rows)
+                     shared_base, T, rows, (const __nv_bfloat16 *)residual)
         : launch_pdl(combine_kernel<float, 4>, grid, dim3(kCombineThreads), 0, s, (const float *)y_perm, pair_row,
-                     gate, (int)K, d, (float *)y, (int)S, shared_base, T, rows);
+                     gate, (int)K, d, (float *)y, (int)S, shared_base, T, rows, (const float *)residual);
     count_launches(1);
     return err;
 }

@@ -215,9 +215,10 @@ cudaError_t launch_scatter_rows(const void *x, const int32_t *pair_row, int64_t 
 cudaError_t launch_imbalance(const int32_t *counts, int64_t T, int64_t N, int64_t M, int32_t *group_load,
                              float *score, cudaStream_t s);
 // y[t] = sum_k gate[t,k] * y_perm[pair_row[t,k]] + sum_{s<S} y_perm[shared_base + s*T + t]
+//        (+ residual[t] when residual is not null)
 cudaError_t launch_combine(const void *y_perm, const int32_t *pair_row, const float *gate, int64_t T,
                            int64_t K, int64_t d, int dtype, void *y, cudaStream_t s, int64_t S = 0,
-                           int64_t shared_base = 0);
+                           int64_t shared_base = 0, const void *residual = nullptr);
 // Rows of S shared experts after the P routed rows: offsets[N+1+s] = P + (s+1)*T and
 // row_token[P + s*T + t] = t (offsets[N] = P is the permutation's).
 cudaError_t launch_shared_rows(int64_t T, int64_t N, int64_t S, int64_t P, int32_t *offsets, int32_t *row_token,

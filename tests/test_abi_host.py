@@ -148,3 +148,21 @@ def test_shared_layer_workspace_and_argument_checks():
     assert f(ctypes.byref(wide), 4, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, big, None) == UNSUPPORTED
     small_ws = moge.moge_workspace_bytes_shared(c, 4) - 256
     assert f(ctypes.byref(c), 4, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, small_ws, None) == WORKSPACE
+
+
+def test_residual_layer_argument_checks():
+    """moge_layer_forward_residual: a residual is required (T > 0) and 16-byte aligned; the rest
+    are moge_layer_forward_shared's checks.  Every call fails before anything is launched."""
+    c = cfg(T=64, N=16, M=4, kpg=1)
+    lib = binding.load()
+    f = lib.moge_layer_forward_residual
+    big = 1 << 40
+    args = lambda res, S=4, ws_bytes=big, cc=c: (ctypes.byref(cc), S, FAKE, res, FAKE, None, FAKE, FAKE, FAKE,  # noqa
+                                                 FAKE, None, FAKE, ws_bytes, None)
+    assert f(*args(None)) == INVALID                     # no residual
+    assert f(*args(FAKE + 8)) == INVALID                 # misaligned residual
+    assert f(*args(FAKE, S=-1)) == INVALID
+    assert f(*args(FAKE, ws_bytes=moge.moge_workspace_bytes_shared(c, 4) - 256)) == WORKSPACE
+    wide = cfg(T=64, N=1024, M=4, kpg=1)
+    assert f(*args(FAKE, cc=wide)) == UNSUPPORTED
+    assert f(None, 0, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE, big, None) == INVALID
