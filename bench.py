@@ -188,7 +188,7 @@ class Layer:
     """Device buffers of one workload and the C-ABI call of one step (with n_shared shared experts
     when n_shared > 0; the weight tensors then hold N + n_shared experts)."""
 
-    def __init__(self, w, d_inp, device, n_shared=0):
+    def __init__(self, w, d_inp, device, n_shared=0, residual=False):
         import torch
         import sparse_router_gemm_global_b300 as moge
         self.moge, self.w, self.dev, self.n_shared = moge, w, device, n_shared
@@ -197,6 +197,8 @@ class Layer:
         self.d = d_inp
         self.x = d_inp["x"][: w.T].contiguous()
         self.y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=device)
+        # residual stream of the same shape (a copy of the tokens; y = r + layer, out of place)
+        self.r = self.x.clone() if residual else None
         self.aux = {"counts": torch.empty(w.N, dtype=torch.int32, device=device),
                     "group_load": torch.empty(w.M, dtype=torch.int32, device=device),
                     "score": torch.empty(4, dtype=torch.float32, device=device)}
@@ -205,7 +207,10 @@ class Layer:
         d = self.d
         x = self.x if x is None else x
         y = self.y if y is None else y
-        if self.n_shared:
+        if self.r is not None:
+            self.moge.moge_layer_forward_residual(self.cfg, self.n_shared, x, self.r, d["w_router"], d["bias"],
+                                                  d["w_gate"], d["w_up"], d["w_down"], y, self.ws, aux=self.aux)
+        elif self.n_shared:
             self.moge.moge_layer_forward_shared(self.cfg, self.n_shared, x, d["w_router"], d["bias"], d["w_gate"],
                                                 d["w_up"], d["w_down"], y, self.ws, aux=self.aux)
         else:
@@ -559,18 +564,19 @@ def run_ours(args):
                             "tflops": round(6.0 * rows * w.d * w.I / (sms / 1e3) / 1e12, 2)}
             del L
 
-    # Pangu Pro MoE's own dimensions: hidden 5120, top-1 per group (K = 8), 4 shared experts
+    # Pangu Pro MoE's own dimensions: hidden 5120, top-1 per group (K = 8), 4 shared experts, the
+    # output added to a residual stream (the whole MoE block of one Pangu Pro layer)
     pangu = None
     if args.pangu_steps > 0:
         pangu = {"n_shared": SHARED_EXPERTS}
         wpp, wpd = WORKLOADS["pangu_k1_t8192"], WORKLOADS["pangu_k1_t32"]
         p_inp = upload(synth.layer_inputs(wpp, seed=DEFAULT_SEED, n_shared=SHARED_EXPERTS), device)
         for name, w, n in (("prefill", wpp, args.pangu_steps), ("decode", wpd, 3 * args.pangu_steps)):
-            L = Layer(w, p_inp, device, n_shared=SHARED_EXPERTS)
+            L = Layer(w, p_inp, device, n_shared=SHARED_EXPERTS, residual=True)
             pms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist, min_warm_s=WARM_S[name])
             rows = w.P + SHARED_EXPERTS * w.T
             touched = int((L.aux["counts"].cpu().numpy() > 0).sum()) + SHARED_EXPERTS
-            pangu[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "d": w.d, "I": w.I, "K": w.K,
+            pangu[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared+residual", "d": w.d, "I": w.I, "K": w.K,
                            "value": round(job_tokens_per_s(w.T, ws_n, pms), 1), "unit": "tokens/s",
                            "ms_per_step": round(pms, 4), "steps": n,
                            "tflops": round(6.0 * rows * w.d * w.I / (pms / 1e3) / 1e12, 2),
