@@ -559,8 +559,8 @@ def run_ours(args):
             L = Layer(w, d_inp, device, n_shared=SHARED_EXPERTS)
             sms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist, min_warm_s=WARM_S[name])
             rows = w.P + SHARED_EXPERTS * w.T
-            shared[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared", "value": round(job_tokens_per_s(w.T, ws_n, sms), 1),
-                            "unit": "tokens/s", "ms_per_step": round(sms, 4), "steps": n,
+            shared[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared",
+                            "value": round(job_tokens_per_s(w.T, ws_n, sms), 1), "unit": "tokens/s", "ms_per_step": round(sms, 4), "steps": n,
                             "tflops": round(6.0 * rows * w.d * w.I / (sms / 1e3) / 1e12, 2)}
             del L
 
