@@ -495,6 +495,8 @@ def cpu_baseline(w, inp, budget_s=10.0):
 
 def run_ours(args):
     import torch
+    for k in WARM_S:
+        WARM_S[k] *= max(args.warm_scale, 0.0)
     ws_n, rank, local = dist_env()
     dist = ws_n > 1
     if dist:
@@ -735,6 +737,8 @@ def main():
     ap.add_argument("--workload", default="prefill_t8192", choices=["prefill_t8192"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
     ap.add_argument("--shared-steps", type=int, default=50, help="steps of the shared-expert layers (0: skip)")
+    ap.add_argument("--warm-scale", type=float, default=1.0,
+                    help="scale of the minimum warm-up times (0: only --warmup steps; for profiling captures)")
     ap.add_argument("--graph-steps", type=int, default=100,
                     help="replays of the step captured as a CUDA graph (decode: 3x; 0: skip)")
     ap.add_argument("--study-batches", type=int, default=1000, help="Monte-Carlo study batches (0: skip)")
