@@ -3,10 +3,12 @@
 // selection inside every group (Pangu Pro MoE explainer, section 1: scores for all experts,
 // one softmax over them, a local top-K' per group).
 //
-// One CTA per (128-token tile, slice of the reduction over d).  128 threads: thread 0 of warp 0
+// One CTA per (128-token tile, slice of the reduction over d).  512 threads: thread 0 of warp 0
 // issues TMA loads, thread 0 of warp 1 issues the MMAs (M = 128 tokens, N = N rounded up to 16
-// experts), then all four warps drain TMEM (warp w owns TMEM lanes 32w..32w+31 = token rows)
-// into shared memory.  The S slices of a tile form one thread-block cluster: after a cluster
+// experts), then all sixteen warps drain TMEM into shared memory (warp w reads TMEM lanes
+// 32(w%4)..+31 = token rows, column chunks w/4, w/4+4, ...).  The epilogue (reduction of the
+// slices, bias, softmax, selection) is latency-bound serial work per row, so it is spread over
+// all sixteen warps: with four it took as long as streaming x through the MMAs.  The S slices of a tile form one thread-block cluster: after a cluster
 // barrier, CTA j adds the S partial tiles for its share of the 128 tokens through distributed
 // shared memory, in slice order (so the result does not depend on timing), and routes those
 // tokens.  No CTA waits on a counter and nothing goes through global memory.
@@ -22,7 +24,7 @@ namespace rt {
 
 using namespace ptx;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;
 constexpr int kBM = kRouterTileRows;   // tokens per tile (MMA M)
 constexpr int kBK = 64;                // bf16 elements per k-block (one 128-byte swizzle row)
 constexpr int kMaxStages = 8;
@@ -121,11 +123,12 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
     bool ok = wait_bar(smem_u32(&tfull_bar), 0, abort_v, p.status);
     ok = __all_sync(0xffffffffu, ok) && !*abort_v;
     tc_fence_after();
-    const int r = warp * 32 + lane;
+    const int quarter = warp & 3;  // TMEM lanes a warp may read: 32 * (warp % 4) ..
+    const int r = quarter * 32 + lane;
     const int stride = p.N + 1;
     float *stage = reinterpret_cast<float *>(smem);  // [128][N+1], reuses the pipeline buffers
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int c0 = 0; c0 < p.npad; c0 += 16) {
+    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+    for (int c0 = (warp >> 2) * 16; c0 < p.npad; c0 += 16 * (kThreads / 128)) {
         uint32_t v[16];
         if (ok) {
             tmem_ld_x16(taddr + c0, v);
@@ -163,21 +166,23 @@ router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
 #pragma unroll
             for (int q = 1; q < kMaxSlices; ++q)
                 if (q < S) acc += v[q];
+            if (p.bias) acc += p.bias[c];
             stage[rr * stride + c] = acc;  // rows [r0, r1) of this CTA are read by no other CTA
+            if (p.logits && t0 + rr < p.T) p.logits[(size_t)(t0 + rr) * p.N + c] = acc;
+        }
+    } else {  // one slice: the bias pass alone
+        for (int i = threadIdx.x; i < (r1 - r0) * p.N; i += kThreads) {
+            const int rr = r0 + i / p.N, c = i - (i / p.N) * p.N;
+            float v = stage[rr * stride + c];
+            if (p.bias) v += p.bias[c];
+            stage[rr * stride + c] = v;
+            if (p.logits && t0 + rr < p.T) p.logits[(size_t)(t0 + rr) * p.N + c] = v;
         }
     }
     __syncthreads();
 
-    // ---- bias, optional scores output, softmax + selection of this CTA's rows
+    // ---- softmax + selection of this CTA's rows
     const int rows = min(r1, ntok) - r0;
-    for (int i = threadIdx.x; i < max(rows, 0) * p.N; i += kThreads) {
-        const int rr = r0 + i / p.N, c = i - (i / p.N) * p.N;
-        float v = stage[rr * stride + c];
-        if (p.bias) v += p.bias[c];
-        stage[rr * stride + c] = v;
-        if (p.logits) p.logits[(size_t)(t0 + rr) * p.N + c] = v;
-    }
-    __syncthreads();
     if (rows > 0)
         route_rows_block(stage, stride, r0, r0 + rows, p.N, p.groups, p.G, p.per, p.idx + (size_t)t0 * (p.groups * p.per),
                          p.gate + (size_t)t0 * (p.groups * p.per), row_max, row_sum);
