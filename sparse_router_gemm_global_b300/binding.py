@@ -60,6 +60,7 @@ def load():
         vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         cfgp = ctypes.POINTER(Config)
         lib.moge_abi_version.restype = i32
+        lib.moge_abi_version.argtypes = []
         lib.moge_status_string.restype = ctypes.c_char_p
         lib.moge_status_string.argtypes = [i32]
         lib.moge_workspace_bytes.restype = sz
@@ -84,6 +85,7 @@ def load():
         lib.moge_imbalance_study.argtypes = [cfgp, ctypes.c_int64, ctypes.c_uint64, vp, vp, vp, vp, vp, vp]
         lib.moge_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         lib.moge_kernel_launch_count.restype = ctypes.c_uint64
+        lib.moge_kernel_launch_count.argtypes = []
         for fn in ("moge_selftest_bounded_wait", "moge_layer_forward_shared", "moge_layer_forward_residual",
                    "moge_imbalance_study", "moge_set_stage_events", "moge_reset_device_status",
                    "moge_query_device_status", "moge_route", "moge_permute", "moge_expert_ffn", "moge_combine",

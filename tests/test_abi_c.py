@@ -83,3 +83,29 @@ def test_header_compiles_as_cpp(tmp_path, program_source):
     cpp.write_text(src.replace("typedef void (*any_fn)(void);", "typedef void (*any_fn)();"))
     subprocess.run(["g++", "-std=c++17", "-fsyntax-only", "-Wall", "-Werror", "-I", INCLUDE, str(cpp)], check=True,
                    capture_output=True, text=True)
+
+
+def declared_parameter_counts():
+    """{function: number of parameters} from the prototypes in include/moge.h."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(moge_\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_declares_every_prototype_with_its_parameter_count():
+    """ctypes trusts argtypes: a binding that passes more or fewer arguments than the C prototype
+    would hand the library garbage.  Every function the binding declares matches the header."""
+    from sparse_router_gemm_global_b300 import binding
+    lib = binding.load()
+    want = declared_parameter_counts()
+    assert len(want) >= 19
+    checked = 0
+    for name, n in want.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes declared"
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+        checked += 1
+    assert checked == len(want)
