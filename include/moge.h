@@ -56,7 +56,7 @@ typedef struct CUstream_st *moge_stream_t; /* same handle as cudaStream_t */
 typedef enum {
     MOGE_OK = 0,
     MOGE_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad shape, N % M != 0, K' outside [1, N/M], misalignment */
-    MOGE_ERR_UNSUPPORTED = 2,      /* dtype/shape combination this build does not handle */
+    MOGE_ERR_UNSUPPORTED = 2,      /* dtype/shape combination the library does not handle */
     MOGE_ERR_WORKSPACE = 3,        /* ws is NULL or ws_bytes < moge_workspace_bytes(cfg) */
     MOGE_ERR_CUDA = 4,             /* a CUDA runtime call or kernel launch failed */
     MOGE_ERR_TIMEOUT = 5           /* a bounded device-side wait gave up (see moge_query_device_status) */
