@@ -38,6 +38,12 @@
  *    it with moge_query_device_status().
  *  - Determinism: every output is bit-reproducible for identical inputs and
  *    configuration (no floating-point atomics; fixed summation orders).
+ *  - CUDA graphs: the layer calls synchronise nothing, allocate nothing and
+ *    read nothing back to the host, so they can be captured into a graph and
+ *    replayed.  The first call on a device sets kernel attributes and looks up
+ *    a driver entry point; make one call of the same kind before capturing.
+ *  - Concurrency: all per-call state lives in the caller's workspace; calls
+ *    on different streams need different workspaces.
  */
 #ifndef MOGE_H
 #define MOGE_H
