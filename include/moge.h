@@ -42,8 +42,13 @@
  *    read nothing back to the host, so they can be captured into a graph and
  *    replayed.  The first call on a device sets kernel attributes and looks up
  *    a driver entry point; make one call of the same kind before capturing.
+ *    moge_permute_noalloc's first call in a context also looks up the address
+ *    of its static scratch array (see there).
  *  - Concurrency: all per-call state lives in the caller's workspace; calls
- *    on different streams need different workspaces.
+ *    on different streams need different workspaces.  The one exception is
+ *    moge_permute_noalloc, whose scratch is a single array inside the library
+ *    shared by all its calls: order those calls on one stream or synchronise
+ *    between them.
  */
 #ifndef MOGE_H
 #define MOGE_H
@@ -160,15 +165,17 @@ moge_status_t moge_permute(const moge_config_t *cfg, const int32_t *topk_idx, co
  * point exists for callers that cannot allocate device memory (a serving
  * runtime whose pool already owns all of HBM and hands a plugin only its input
  * and output buffers, or a latency-critical loop that must not call cudaMalloc,
- * which can synchronise the device).  Arguments, outputs and errors are those
- * of moge_permute minus ws/ws_bytes.
+ * which can synchronise the device).  Arguments, outputs, checks and errors
+ * are those of moge_permute minus ws/ws_bytes.
  *   Scratch: a static device array of 256 KiB inside the library (held by every
  *   GPU that loads it until the process exits), enough for
  *   ceil(T/256) * N <= 65536 (e.g. T <= 16384 with N <= 256); larger problems
  *   return MOGE_ERR_UNSUPPORTED before anything is launched.
- *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   The first call in each CUDA context (normally a device's primary context)
+ *   looks up the array's device address in that context (cudaGetSymbolAddress)
+ *   and remembers it for the context; make that first call before any stream
+ *   capture.  After cudaDeviceReset the remembered address belongs to a context
+ *   that no longer exists: do not call this entry point in that process again.
  *   All calls share the array and it keeps the last call's contents (nothing in
  *   it needs to start at zero): calls that overlap on the GPU race, so order
  *   them on one stream or synchronise between them.

@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "ffn_tc.cuh"
+#include "validate.cuh"
 
 using namespace moge;
 
@@ -42,40 +43,13 @@ void mark_stage(int stage, cudaStream_t s) {
 
 namespace {
 
-constexpr int64_t kMaxExperts = 1024;
-constexpr int64_t kMaxSlots = 1024;
-
-bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+constexpr int64_t kMaxExperts = kAbiMaxExperts;
 
 moge_status_t cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return MOGE_OK;
     static bool verbose = getenv("MOGE_VERBOSE") != nullptr;
     if (verbose) fprintf(stderr, "moge: CUDA error %s\n", cudaGetErrorString(e));
     return MOGE_ERR_CUDA;
-}
-
-// Routing shape: T >= 0, 1 <= M, N % M == 0, 1 <= K' <= N/M, N <= 1024, T*K < 2^31.
-moge_status_t check_routing(const moge_config_t *c) {
-    if (!c) return MOGE_ERR_INVALID_ARGUMENT;
-    if (c->T < 0 || c->N < 1 || c->M < 1 || c->N % c->M != 0) return MOGE_ERR_INVALID_ARGUMENT;
-    if (c->k_per_group < 1 || c->k_per_group > c->N / c->M) return MOGE_ERR_INVALID_ARGUMENT;
-    const int64_t K = c->M * c->k_per_group;
-    if (c->N > kMaxExperts || K > kMaxSlots) return MOGE_ERR_UNSUPPORTED;
-    if (c->T > ((int64_t)1 << 31) / K - 1) return MOGE_ERR_UNSUPPORTED;
-    return MOGE_OK;
-}
-
-// Full layer shape: routing shape + d, I >= 1, one supported dtype, 16-byte rows.
-moge_status_t check_layer(const moge_config_t *c) {
-    moge_status_t s = check_routing(c);
-    if (s != MOGE_OK) return s;
-    if (c->d < 1 || c->I < 1) return MOGE_ERR_INVALID_ARGUMENT;
-    if (c->act_dtype != c->weight_dtype) return MOGE_ERR_UNSUPPORTED;
-    if (c->act_dtype != MOGE_F32 && c->act_dtype != MOGE_BF16) return MOGE_ERR_UNSUPPORTED;
-    const int64_t vec = (c->act_dtype == MOGE_BF16) ? 8 : 4;  // elements per 16 bytes
-    if (c->d % vec != 0 || c->I % vec != 0) return MOGE_ERR_UNSUPPORTED;
-    if (c->d > (1 << 20) || c->I > (1 << 20)) return MOGE_ERR_UNSUPPORTED;
-    return MOGE_OK;
 }
 
 moge_status_t check_ws(const moge_config_t *c, void *ws, size_t ws_bytes, int64_t S = 0) {
@@ -273,13 +247,8 @@ moge_status_t moge_permute(const moge_config_t *cfg, const int32_t *topk_idx, co
                            int32_t *offsets, int32_t *pair_row, int32_t *row_token, void *x_perm, void *ws,
                            size_t ws_bytes, moge_stream_t stream) {
     const bool gather = x && x_perm;
-    moge_status_t s = gather ? check_layer(cfg) : check_routing(cfg);
+    moge_status_t s = check_permute_args(cfg, topk_idx, x, counts, offsets, pair_row, row_token, x_perm);
     if (s != MOGE_OK) return s;
-    if (!topk_idx || !counts || !offsets) return MOGE_ERR_INVALID_ARGUMENT;
-    if (gather && !row_token) return MOGE_ERR_INVALID_ARGUMENT;
-    for (const void *p : {(const void *)topk_idx, x, (const void *)counts, (const void *)offsets,
-                          (const void *)pair_row, (const void *)row_token, (const void *)x_perm})
-        if (p && !aligned16(p)) return MOGE_ERR_INVALID_ARGUMENT;
     if ((s = check_ws(cfg, ws, ws_bytes)) != MOGE_OK) return s;
     const WsLayout L = ws_layout(*cfg);
     const int64_t K = cfg->M * cfg->k_per_group;

@@ -9,37 +9,67 @@
 // library holds it (kNoAllocScratchBytes) until the process exits.
 //
 // Host code may not use the array's name as a device address (on the host it names a
-// stand-in object); its device address is taken with cudaGetSymbolAddress once per device,
-// with that device current, on the first call made on that device.
+// stand-in object); its device address is taken with cudaGetSymbolAddress once per CUDA context,
+// with that context current, on the first call made in it.  The cache is keyed on the current
+// driver context (cuCtxGetCurrent, looked up through the runtime like the tensor-map encoder),
+// so a caller that makes its own context current on a device gets that context's address, not
+// the primary context's.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
+#include "validate.cuh"
 
 namespace moge {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 256 * 1024;  // chunks * N int32 counts
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
-std::mutex g_mutex;
-int32_t *g_scratch_ptr[kMaxDevices] = {};
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
 
-// Device address of g_permute_scratch on the current device (nullptr on failure).
-int32_t *scratch_on_current_device() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_permute_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = static_cast<int32_t *>(ptr);
-    }
-    return g_scratch_ptr[dev];
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    });
+    return fn;
 }
 
-bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+std::mutex g_mutex;
+struct CachedAddress {
+    CUcontext ctx;
+    int32_t *ptr;
+};
+CachedAddress g_cache[kMaxContexts] = {};
+int g_cached = 0;
+
+// Device address of g_permute_scratch in the current context (nullptr on failure).
+int32_t *scratch_in_current_context() {
+    CtxGetCurrentFn get = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (ctx)
+        for (int i = 0; i < g_cached; ++i)
+            if (g_cache[i].ctx == ctx) return g_cache[i].ptr;
+    // first call in this context; with no context current yet, the lookup itself makes the
+    // current device's primary context current (as every runtime call does), then it is read
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_permute_scratch) != cudaSuccess || !ptr) return nullptr;
+    if (!ctx && (get(&ctx) != CUDA_SUCCESS || !ctx)) return nullptr;
+    if (g_cached < kMaxContexts) g_cache[g_cached++] = {ctx, static_cast<int32_t *>(ptr)};
+    return static_cast<int32_t *>(ptr);
+}
 
 }  // namespace
 }  // namespace moge
@@ -48,27 +78,16 @@ extern "C" moge_status_t moge_permute_noalloc(const moge_config_t *cfg, const in
                                               int32_t *counts, int32_t *offsets, int32_t *pair_row,
                                               int32_t *row_token, void *x_perm, moge_stream_t stream) {
     using namespace moge;
-    if (!cfg) return MOGE_ERR_INVALID_ARGUMENT;
+    // the same checks as moge_permute
+    moge_status_t s = check_permute_args(cfg, topk_idx, x, counts, offsets, pair_row, row_token, x_perm);
+    if (s != MOGE_OK) return s;
     const moge_config_t &c = *cfg;
-    if (c.T < 0 || c.N < 1 || c.M < 1 || c.N % c.M != 0) return MOGE_ERR_INVALID_ARGUMENT;
-    if (c.k_per_group < 1 || c.k_per_group > c.N / c.M) return MOGE_ERR_INVALID_ARGUMENT;
     const int64_t K = c.M * c.k_per_group;
-    if (c.N > 1024 || K > 1024 || c.T > ((int64_t)1 << 31) / K - 1) return MOGE_ERR_UNSUPPORTED;
     const bool gather = x && x_perm;
-    if (gather) {
-        if (c.d < 1) return MOGE_ERR_INVALID_ARGUMENT;
-        if (c.act_dtype != MOGE_F32 && c.act_dtype != MOGE_BF16) return MOGE_ERR_UNSUPPORTED;
-        if (c.d % (c.act_dtype == MOGE_BF16 ? 8 : 4) != 0) return MOGE_ERR_UNSUPPORTED;
-        if (!row_token) return MOGE_ERR_INVALID_ARGUMENT;
-    }
-    if (!topk_idx || !counts || !offsets) return MOGE_ERR_INVALID_ARGUMENT;
-    for (const void *p : {(const void *)topk_idx, x, (const void *)counts, (const void *)offsets,
-                          (const void *)pair_row, (const void *)row_token, (const void *)x_perm})
-        if (p && !aligned16(p)) return MOGE_ERR_INVALID_ARGUMENT;
     // the static array bounds the problem size: one int32 count per (token chunk, expert)
     const int64_t chunks = cdiv(c.T > 0 ? c.T : 1, kPermuteChunk);
     if ((size_t)(chunks * c.N) * sizeof(int32_t) > kNoAllocScratchBytes) return MOGE_ERR_UNSUPPORTED;
-    int32_t *scratch = scratch_on_current_device();
+    int32_t *scratch = scratch_in_current_context();
     if (!scratch) return MOGE_ERR_CUDA;
     // Every count the scan reads is written earlier in the same call, so nothing in the array
     // has to start at zero; calls that overlap on the GPU share the array and race.

@@ -77,6 +77,29 @@ def max_rel_err(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-300))
 
 
+def expert_covering_tokens(offsets, row_token, T, step=128):
+    """Tokens whose rows reach every tile of every touched expert.
+
+    For each expert e with rows [offsets[e], offsets[e+1]): its first row, its last row and the
+    first row of every `step`-row block after the first (so both halves of every 256-row
+    CTA-pair tile and every short last block are hit), mapped to tokens through row_token; plus
+    tokens 0 and T-1.  Returns (sorted token array, number of touched experts)."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    rows = []
+    touched = 0
+    for e in range(len(offsets) - 1):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b <= a:
+            continue
+        touched += 1
+        rows.extend(range(a, b, step))
+        rows.append(b - 1)
+    toks = set(int(row_token[r]) for r in rows)
+    toks.update({0, T - 1})
+    toks = np.array(sorted(toks), dtype=np.int32)
+    return toks, touched
+
+
 def routing_mismatch_ok(idx_gpu, idx_ref, p_ref, M, kpg, gap=1e-6):
     """Tokens whose routing differs from the oracle's.  Every differing slot must
     be a near-tie: the oracle's softmax probabilities of the two experts in that

@@ -12,8 +12,8 @@ import torch
 import oracle
 import sparse_router_gemm_global_b300 as moge
 import synth
-from gpu_util import (DEV, as_f64, config, dev, host, max_rel_err, routing_mismatch_ok, run_layer,
-                      torch_dtype, upload_layer)
+from gpu_util import (DEV, as_f64, config, dev, expert_covering_tokens, host, max_rel_err, routing_mismatch_ok,
+                      run_layer, torch_dtype, upload_layer)
 from synth import WORKLOADS
 
 pytestmark = pytest.mark.gpu
@@ -45,6 +45,20 @@ def check_layer(w, inp, got, tokens=None, seed_note=""):
                                   inp["w_down"])
     err = max_rel_err(got["y"][toks], y_ref)
     assert err <= TOL[w.dtype], f"{w.name}: max rel err {err:.3e} {seed_note}"
+    return err, toks
+
+
+def check_layer_every_expert(w, inp, got):
+    """check_layer on the tokens that reach every tile of every touched expert (first and last
+    row, and one row in every 128-row block, of each expert's segment of the GPU's permutation):
+    every expert the batch touches has its output rows compared."""
+    perm = oracle.permute(got["topk_idx"], w.N)
+    toks, touched = expert_covering_tokens(perm["offsets"], perm["row_token"], w.T)
+    err, compared = check_layer(w, inp, got, tokens=toks)
+    checked = np.unique(got["topk_idx"][compared])
+    print(f"{w.name}: {len(compared)} tokens compared, {len(checked)} of {touched} touched experts, "
+          f"max rel err {err:.3e}")
+    assert len(checked) == touched == int(np.count_nonzero(perm["counts"]))
     return err
 
 
@@ -81,13 +95,11 @@ def test_decode_t32_full():
     check_layer(w, inp, got)
 
 
-def test_prefill_t8192_sampled():
+def test_prefill_t8192_every_expert():
     w = WORKLOADS["prefill_t8192"]
     inp = synth.layer_inputs(w)
     got = run_layer(w, upload_layer(inp))
-    rng = np.random.default_rng(1)
-    toks = np.sort(np.concatenate([[0, w.T - 1], rng.choice(w.T, 46, replace=False)]))
-    check_layer(w, inp, got, tokens=toks)
+    check_layer_every_expert(w, inp, got)
 
 
 def test_layer_is_deterministic():
@@ -141,13 +153,11 @@ def test_empty_layer():
 
 
 @pytest.mark.slow
-def test_stress_n256_sampled():
+def test_stress_n256_every_expert():
     w = WORKLOADS["stress_n256"]
     inp = synth.layer_inputs(w)
     got = run_layer(w, upload_layer(inp))
-    rng = np.random.default_rng(2)
-    toks = np.sort(rng.choice(w.T, 24, replace=False))
-    check_layer(w, inp, got, tokens=toks)
+    check_layer_every_expert(w, inp, got)
 
 
 @pytest.mark.parametrize("T", [16, 17, 32, 33, 64, 65, 128, 192, 193, 256, 257, 384, 416, 417])
@@ -254,9 +264,8 @@ def test_layer_with_1024_experts():
 @pytest.mark.slow
 def test_layer_with_half_a_million_rows():
     """T=32768 tokens x K=16: 524288 (token, expert) rows, ~2000 CTA-pair tiles per GEMM;
-    every token's routing checked, 40 sampled output rows."""
+    every token's routing checked, output rows of tokens reaching every tile of every expert."""
     w = WORKLOADS["prefill_t8192"].with_(name="rows512k", T=32768, d=256, I=128)
     inp = synth.layer_inputs(w, seed=32)
     got = run_layer(w, upload_layer(inp))
-    toks = np.sort(np.random.default_rng(4).choice(w.T, 40, replace=False))
-    check_layer(w, inp, got, tokens=toks)
+    check_layer_every_expert(w, inp, got)

@@ -120,14 +120,29 @@ def test_bf16_arrays_read_as_exact_values():
     np.testing.assert_array_equal(a["y"], b["y"])
 
 
+def identical_experts_residual(w, seed, gate_fn):
+    """max |y - (sum_k p_k) FFN(x)| / max |y| for a layer whose experts all share one set of
+    weights, y computed by the oracle's combine with gates gate_fn(oracle gates)."""
+    inp = synth.layer_inputs(w, seed=seed)
+    for k in ("w_gate", "w_up", "w_down"):
+        inp[k] = np.ascontiguousarray(np.broadcast_to(inp[k][:1], inp[k].shape))
+    r = oracle.route(oracle.router_logits(inp["x"], inp["w_router"], inp["bias"]), w.M, w.kpg)
+    toks = np.arange(w.T)
+    y = oracle.combine_tokens(toks, r["idx"], gate_fn(r["gate64"]), inp["x"], inp["w_gate"], inp["w_up"],
+                              inp["w_down"])
+    f = oracle.expert_ffn_pairs(toks, np.zeros(w.T), inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
+    expect = r["gate64"].sum(axis=1)[:, None] * f
+    return np.max(np.abs(y - expect)) / np.max(np.abs(expect))
+
+
 def test_planted_renormalised_gates_mistake_is_caught():
-    # renormalising gates over the selection (a plausible misreading) breaks the
-    # identical-experts closed form with unrenormalised probabilities
-    w = WORKLOADS["tiny_fp32"].with_(T=8, d=32, I=16)
-    inp = synth.layer_inputs(w, seed=6)
-    r = oracle.route(oracle.router_logits(inp["x"], inp["w_router"]), w.M, w.kpg)
-    renorm = r["gate64"] / r["gate64"].sum(axis=1, keepdims=True)
-    assert np.max(np.abs(renorm.sum(axis=1) - r["gate64"].sum(axis=1))) > 0.1
+    # The closed-form check of test_identical_experts_closed_form, run on a planted variant of the
+    # combine that renormalises the gates over the selected experts (a plausible misreading of
+    # the explainer's section 1, which keeps the global-softmax probabilities): the check accepts
+    # the oracle's gates and rejects the variant's by orders of magnitude.
+    w = WORKLOADS["tiny_fp32"].with_(T=16, d=32, I=16)
+    assert identical_experts_residual(w, 6, lambda g: g) < 1e-12
+    assert identical_experts_residual(w, 6, lambda g: g / g.sum(axis=1, keepdims=True)) > 0.1
 
 
 def test_combine_rows_equals_per_token_combine():
