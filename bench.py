@@ -428,21 +428,25 @@ def imbalance_study(batches, device):
                             "max": round(float(glob.max()), 4), "frac_above_zero": float((glob > 0).mean())}}
 
 
-def gate_up_roofline(w, counts, stage_ms, pk, peak_kind):
-    """Roofline of the dominant kernel (grouped gate/up GEMM + SwiGLU) from its stage time."""
+def gate_up_roofline(w, counts, stage_ms, pk, peak_kind, sm_mhz=None):
+    """Roofline of the dominant kernel (grouped gate/up GEMM + SwiGLU) from its launch time in the
+    timed region.  Tensor-bound shapes: `frac` against the measured burst bf16 figure (cuBLAS timed
+    alone), `frac_sustained` against the seconds-long power-capped figure, and the SM clock
+    sampled in the timed region beside the clock the sustained figure was measured at (the
+    sustained denominator is only comparable at the same clock)."""
     P = w.P
     touched = int((counts > 0).sum())
     flops = 4.0 * P * w.d * w.I
     bytes_alg = touched * 2 * w.I * w.d * 2 + P * w.d * 2 + P * w.I * 2
     sec = stage_ms / 1e3
     if w.T >= 1024:  # tensor-core bound shape
-        # the kernel runs inside a long back-to-back step loop (power capped), so the
-        # sustained bf16 figure is its peak; the burst fraction is given beside it
         achieved = flops / sec / 1e12
-        peak = pk["bf16_tflops_sustained"]
+        peak = pk["bf16_tflops"]
         rl = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-              "frac": round(achieved / peak, 4), "peak_kind": f"bf16 sustained, {peak_kind}",
-              "frac_of_burst": round(achieved / pk["bf16_tflops"], 4),
+              "frac": round(achieved / peak, 4), "peak_kind": f"bf16 burst, {peak_kind}",
+              "frac_sustained": round(achieved / pk["bf16_tflops_sustained"], 4),
+              "sm_mhz_timed_region": sm_mhz,
+              "sm_mhz_of_sustained_peak": (pk.get("clocks_under_load") or {}).get("sm_mhz_median"),
               "algorithmic_per_launch": {"flop": flops}, "kernel": "gate_up grouped GEMM + SwiGLU"}
     else:
         achieved = bytes_alg / sec / 1e9
@@ -457,40 +461,202 @@ def gate_up_roofline(w, counts, stage_ms, pk, peak_kind):
 
 
 def layer_roofline(w, counts, ms, pk):
-    """Whole-layer fractions for context: FLOP vs TC peak and touched weight bytes vs HBM peak."""
+    """Whole-layer fractions: FLOP (grouped GEMMs + router) against the bf16 peaks (burst and
+    sustained), touched expert weight bytes against the HBM peak, and the fraction of the
+    max(tensor time, HBM time) roofline."""
     touched = int((counts > 0).sum())
     flops = 6.0 * w.P * w.d * w.I + 2.0 * w.T * w.d * w.N
     wbytes = touched * 3 * w.I * w.d * 2
     sec = ms / 1e3
+    t_roof = max(flops / (pk["bf16_tflops"] * 1e12), wbytes / (pk["hbm_gbs"] * 1e9))
     return {"tflops": round(flops / sec / 1e12, 2),
-            "tc_frac": round(flops / sec / 1e12 / pk["bf16_tflops_sustained"], 4),
+            "tc_frac": round(flops / sec / 1e12 / pk["bf16_tflops"], 4),
+            "tc_frac_sustained": round(flops / sec / 1e12 / pk["bf16_tflops_sustained"], 4),
             "weight_gbs": round(wbytes / sec / 1e9, 1), "hbm_frac": round(wbytes / sec / 1e9 / pk["hbm_gbs"], 4),
-            "touched_experts": touched}
+            "roofline_ms": round(t_roof * 1e3, 4), "roofline_frac": round(t_roof / sec, 4),
+            "touched_experts": touched, "flop": flops, "weight_bytes": wbytes}
 
 
-def cpu_baseline(w, inp, budget_s=10.0):
-    """The oracle as it stands, on this host's cores: routing of every token plus the
-    expert FFN + combine of a token sample sized to ~budget_s; tokens/s extrapolated."""
+def _time_loop(step, steps, min_warm_s=0.1):
+    """ms per call of step() from CUDA events around `steps` calls, after at least 3 calls and
+    min_warm_s seconds of warm-up."""
+    import torch
+    t0 = time.perf_counter()
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    while time.perf_counter() - t0 < min_warm_s:
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def routing_bench(steps, device, pk):
+    """The routing workload (Pangu Pro MoE explainer, section 1): 16384 tokens, fp32 scores
+    N(0,1) + the popularity bias over 64 experts in 8 groups.  One step = moge_route from the
+    given scores + moge_permute (counts, offsets, pair rows, row tokens) + moge_imbalance_score,
+    for MoGE routing at K'=2 and K'=1 and for plain global top-K (K = 16, 8) on the same scores.
+    The 4 MiB of scores and the outputs stay in L2 between steps (stated, not flushed)."""
+    import torch
+    import sparse_router_gemm_global_b300 as moge
+    w = WORKLOADS["routing_16k"]
+    logits = torch.from_numpy(synth.route_logits(DEFAULT_SEED, w.T, w.N)).to(device)
+    out = {"workload": w.name, "T": w.T, "N": w.N, "M": w.M, "unit": "tokens/s", "steps": steps,
+           "step": "moge_route (given fp32 scores) + moge_permute (no row copy) + moge_imbalance_score",
+           "l2": "L2-resident: 4 MiB of scores, at most 7 MiB of outputs"}
+    i32 = torch.int32
+    for kpg in (2, 1):
+        c = moge.make_config(w.T, 0, w.N, w.M, kpg, 0, "f32")
+        ws = moge.alloc_workspace(c, device)
+        K = w.M * kpg
+        idx = torch.empty((w.T, K), dtype=i32, device=device)
+        gate = torch.empty((w.T, K), dtype=torch.float32, device=device)
+        counts = torch.empty(w.N, dtype=i32, device=device)
+        offsets = torch.empty(w.N + 1, dtype=i32, device=device)
+        pair_row = torch.empty((w.T, K), dtype=i32, device=device)
+        row_token = torch.empty(w.T * K, dtype=i32, device=device)
+        loads = torch.empty(w.M, dtype=i32, device=device)
+        score = torch.empty(4, dtype=torch.float32, device=device)
+        for mode, name in ((moge.MOGE_ROUTE_GROUPED, f"moge_k{kpg}"), (moge.MOGE_ROUTE_GLOBAL_TOPK, f"global_top{K}")):
+            def step():
+                moge.moge_route(c, mode, None, None, None, logits, idx, gate, ws)
+                moge.moge_permute(c, idx, None, counts, offsets, pair_row, row_token, None, ws)
+                moge.moge_imbalance_score(c, counts, loads, score)
+            ms = _time_loop(step, steps)
+            # bytes each step must move at least: scores in, idx + gate + pair_row + row_token out
+            alg = w.T * w.N * 4 + 4 * w.T * K * 4
+            out[name] = {"K": K, "ms_per_step": round(ms, 5), "value": round(w.T / (ms / 1e3), 1),
+                         "imbalance_score": round(float(score[0].item()), 5),
+                         "gbs": round(alg / (ms / 1e3) / 1e9, 1),
+                         "hbm_frac": round(alg / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+        del ws
+    return out
+
+
+def tiny_bench(steps, device):
+    """The tiny all-fp32 layer (T=64, d=256, N=16 in 4 groups, K'=1, I=128; CUDA-core FMA path):
+    one moge_layer_forward per step, inputs resident and L2-resident (6.3 MB of weights)."""
+    import torch
+    import sparse_router_gemm_global_b300 as moge
+    w = WORKLOADS["tiny_fp32"]
+    d = upload(synth.layer_inputs(w, seed=DEFAULT_SEED), device)
+    c = moge.make_config(w.T, w.d, w.N, w.M, w.kpg, w.I, w.dtype)
+    ws = moge.alloc_workspace(c, device)
+    y = torch.empty((w.T, w.d), dtype=torch.float32, device=device)
+
+    def step():
+        moge.moge_layer_forward(c, d["x"], d["w_router"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], y, ws)
+    ms = _time_loop(step, steps)
+    return {"workload": w.name, "dtype": "f32", "value": round(w.T / (ms / 1e3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms, 5), "steps": steps, "l2": "L2-resident (6.3 MB of fp32 weights)"}
+
+
+def stress_bench(steps, warmup, dist, device, pk, ws_n):
+    """The large-sparse stress layer (T=4096, d=7680, N=256 in 8 groups of 32, K'=1, I=2048; the
+    dimensions of the Pangu Ultra MoE page with MoGE routing imposed): one moge_layer_forward per
+    step, 24 GB of expert weights resident (larger than L2).  Both roofline fractions: FLOP of the
+    grouped GEMMs + router against the bf16 peaks, and the weight bytes of the touched experts
+    against the HBM peak; `roofline_frac` = max(tensor time, HBM time) / step time."""
+    w = WORKLOADS["stress_n256"]
+    inp = synth.layer_inputs(w, seed=DEFAULT_SEED)
+    d_inp = upload(inp, device)
+    del inp
+    L = Layer(w, d_inp, device)
+    ms, _, launches = timed_steps(L, steps, warmup, dist, min_warm_s=WARM_S["prefill"])
+    counts = L.aux["counts"].cpu().numpy()
+    res = {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "M": w.M, "k_per_group": w.kpg, "K": w.K, "I": w.I,
+           "value": round(job_tokens_per_s(w.T, ws_n, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+           "steps": steps, "gpu_launches": int(launches), "rows_per_expert_max": int(counts.max()),
+           "experts_with_at_most_128_rows": int(((counts > 0) & (counts <= 128)).sum()),
+           "layer_roofline": layer_roofline(w, counts, ms, pk)}
+    del L, d_inp
+    return res
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def oracle_layer_rate(w, inp, n_ffn, rng):
+    """The oracle on one workload: routing of all T tokens (the permutation needs every token),
+    then the expert FFN + combine of n_ffn tokens (all T when n_ffn >= T, else a seeded sample).
+    Returns (seconds per token with the FFN cost extrapolated to T, routing s, FFN s, FFN tokens)."""
     import oracle
-    cores = oracle.num_threads()
     t0 = time.perf_counter()
-    logits = oracle.router_logits(inp["x"], inp["w_router"], inp["bias"])
-    r = oracle.route(logits, w.M, w.kpg)
+    r = oracle.route(oracle.router_logits(inp["x"], inp["w_router"], inp["bias"]), w.M, w.kpg)
     t_route = time.perf_counter() - t0
-    probe = np.arange(min(4, w.T), dtype=np.int32)
-    t0 = time.perf_counter()
-    oracle.combine_tokens(probe, r["idx"], r["gate64"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
-    per_tok = (time.perf_counter() - t0) / len(probe)
-    n = int(max(len(probe), min(w.T, budget_s / max(per_tok, 1e-9))))
-    rng = np.random.default_rng(0)
-    sample = np.sort(rng.choice(w.T, n, replace=False)).astype(np.int32)
+    n = min(max(1, n_ffn), w.T)
+    sample = np.arange(w.T, dtype=np.int32) if n == w.T else \
+        np.sort(rng.choice(w.T, n, replace=False)).astype(np.int32)
     t0 = time.perf_counter()
     oracle.combine_tokens(sample, r["idx"], r["gate64"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
     t_ffn = time.perf_counter() - t0
-    sec_per_token = t_route / w.T + t_ffn / n
-    return {"value": round(1.0 / sec_per_token, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{w.name}: routing of all {w.T} tokens ({t_route:.2f} s) + expert FFN and combine of "
-                      f"{n} sampled tokens ({t_ffn:.2f} s), per-token cost extrapolated to T={w.T}"}
+    return t_route / w.T + t_ffn / n, t_route, t_ffn, n
+
+
+REF_TOKENS_PER_THREAD = 4  # oracle FFN tokens per thread in a reference-arm step
+
+
+def cpu_baseline(w, inp, wd, budget_s=8.0):
+    """The oracle as it stands on this host's cores, at every thread and at one thread: the
+    prefill layer (routing of every token + the FFN of a token sample sized to ~budget_s,
+    extrapolated per token) and the decode layer in full (all threads; one thread: a sample)."""
+    import oracle
+    cores = oracle.num_threads()
+    rng = np.random.default_rng(0)
+    d_inp = {k: (v[: wd.T] if k == "x" else v) for k, v in inp.items()}
+    res = {"unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model()}
+    try:
+        for threads in (cores, 1):
+            oracle.set_num_threads(threads)
+            # prefill FFN sample: REF_TOKENS_PER_THREAD tokens per thread (the reference arm's
+            # sample, so that the two agree), more while a 2-token probe says budget_s allows
+            # (a quarter of it at one thread), always a whole number of tokens per thread
+            _, _, t_probe, _ = oracle_layer_rate(wd, d_inp, 2, rng)
+            budget = budget_s if threads > 1 else budget_s / 4
+            per_thread = max(REF_TOKENS_PER_THREAD, int(budget / max(t_probe / 2, 1e-9) / threads))
+            n = int(min(w.T, threads * per_thread if threads > 1 else 3))
+            sec, t_route, t_ffn, n = oracle_layer_rate(w, inp, n, rng)
+            dn = wd.T if threads > 1 else 4
+            dsec, dt_route, dt_ffn, dn = oracle_layer_rate(wd, d_inp, dn, rng)
+            key = "threads_all" if threads > 1 else "threads_1"
+            res[key] = {
+                "threads": threads,
+                "prefill": {"value": round(1.0 / sec, 3), "route_s": round(t_route, 3), "ffn_s": round(t_ffn, 3),
+                            "ffn_tokens": n, "extrapolated": n < w.T},
+                "decode": {"value": round(1.0 / dsec, 3), "route_s": round(dt_route, 4), "ffn_s": round(dt_ffn, 3),
+                           "ffn_tokens": dn, "extrapolated": dn < wd.T}}
+    finally:
+        oracle.set_num_threads(cores)
+    res["value"] = res["threads_all"]["prefill"]["value"]
+    a = res["threads_all"]["prefill"]
+    res["sample"] = (f"{w.name}: routing of all {w.T} tokens + expert FFN and combine of {a['ffn_tokens']} sampled "
+                     f"tokens on {cores} threads, per-token cost extrapolated to T={w.T}; {wd.name} in full; "
+                     f"threads_1: the same at one thread (prefill and decode FFN on samples)")
+    return res
+
+
+def workload_config(w, ws_n):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "M": w.M, "k_per_group": w.kpg, "K": w.K, "I": w.I,
+            "seed": DEFAULT_SEED, "parallelism": f"replicas x{ws_n}",
+            "l2": "inputs larger than L2 (2.2 GB of expert weights, 1 GB permuted activations)"}
 
 
 def run_ours(args):
@@ -543,7 +709,7 @@ def run_ours(args):
                   "ms_per_step": round(dms, 4), "steps": args.decode_steps,
                   "roofline": gate_up_roofline(wd, dcounts, dgate_up_ms, pk, peak_kind),
                   "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
-                  "stage_ms": dstages, "cuda_graph": dgraph, "gpu_launches": int(dlaunches)}
+                  "stage_share_ms": dstages, "cuda_graph": dgraph, "gpu_launches": int(dlaunches)}
 
     # the prefill step captured as a CUDA graph (after the decode timing: its replays are a
     # seconds-long load that would leave the short decode window starting power-throttled)
@@ -562,7 +728,8 @@ def run_ours(args):
             sms, _, _ = timed_steps(L, n, max(args.warmup, 3), dist, min_warm_s=WARM_S[name])
             rows = w.P + SHARED_EXPERTS * w.T
             shared[name] = {"workload": f"{w.name}+{SHARED_EXPERTS}shared",
-                            "value": round(job_tokens_per_s(w.T, ws_n, sms), 1), "unit": "tokens/s", "ms_per_step": round(sms, 4), "steps": n,
+                            "value": round(job_tokens_per_s(w.T, ws_n, sms), 1), "unit": "tokens/s",
+                            "ms_per_step": round(sms, 4), "steps": n,
                             "tflops": round(6.0 * rows * w.d * w.I / (sms / 1e3) / 1e12, 2)}
             del L
 
@@ -592,6 +759,10 @@ def run_ours(args):
     if args.study_batches > 0:
         study = imbalance_study(args.study_batches, device)
 
+    # the routing workload (route + permute + imbalance score) and the tiny all-fp32 layer
+    routing = routing_bench(args.routing_steps, device, pk) if args.routing_steps > 0 else None
+    tiny = tiny_bench(args.tiny_steps, device) if args.tiny_steps > 0 else None
+
     # end to end through the public call with host buffers
     e2e = None
     if not args.no_e2e:
@@ -599,6 +770,13 @@ def run_ours(args):
         e2e = {"value": round(job_tokens_per_s(wp.T, ws_n, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                "copies": "pinned host buffers; upload of step i+1 and download of step i-1 overlap step i"}
+
+    # the large-sparse stress layer (24 GB of weights, generated last so the other layers' inputs
+    # are released first)
+    stress = None
+    if args.stress_steps > 0:
+        del prefill, d_inp
+        stress = stress_bench(args.stress_steps, max(args.warmup, 3), dist, device, pk, ws_n)
 
     res = {
         "metric": METRIC,
@@ -615,12 +793,13 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded splitmix64 + Box-Muller; random-init weights N(0,1/fan_in), "
                 "router bias 1.5 ln(1/rank_e))",
-        "config": {"workload": wp.name, "T": wp.T, "d": wp.d, "N": wp.N, "M": wp.M, "k_per_group": wp.kpg,
-                   "K": wp.K, "I": wp.I, "seed": DEFAULT_SEED, "parallelism": f"replicas x{ws_n}",
-                   "l2": "inputs larger than L2 (2.2 GB of expert weights, 1 GB permuted activations)"},
-        "roofline": gate_up_roofline(wp, counts, gate_up_ms, pk, peak_kind),
+        "config": workload_config(wp, ws_n),
+        "roofline": gate_up_roofline(wp, counts, gate_up_ms, pk, peak_kind, sm_mhz=clocks.get("sm_mhz")),
         "layer_roofline": layer_roofline(wp, counts, ms, pk),
-        "stage_ms": stages,
+        "stage_share_ms": stages,
+        "stage_share_note": ("stage durations from a separate pass with events at every stage boundary "
+                             "(those events break the launch overlap): shares of the step, not absolute "
+                             "times in the timed region"),
         "cuda_graph": graph,
         "imbalance_score": score,
         "clocks": clocks,
@@ -630,9 +809,12 @@ def run_ours(args):
         "shared_experts": shared,
         "pangu_dims_k1": pangu,
         "imbalance_study": study,
+        "stress": stress,
+        "routing": routing,
+        "tiny_fp32": tiny,
     }
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(wp, inp, budget_s=args.cpu_budget)
+        res["cpu_baseline"] = cpu_baseline(wp, inp, wd, budget_s=args.cpu_budget)
     if dist:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -645,6 +827,11 @@ def run_ours(args):
 # --------------------------------------------------------------------------------------------
 
 def run_reference(args):
+    """The CPU oracle as it stands, on the host cores.  Each step routes all T tokens and runs the
+    expert FFN + combine of a token sample (4 tokens per oracle thread by default, so that every
+    core works, as in the CPU baseline of our arm); `ms_per_step` is the wall time of the step
+    actually run, and the per-token cost extrapolated to a whole T-token layer is reported
+    separately as `extrapolated_layer_ms`."""
     ws_n, rank, _ = dist_env()
     if rank != 0:
         return
@@ -653,36 +840,31 @@ def run_reference(args):
     inp = synth.layer_inputs(w, seed=DEFAULT_SEED)
     cores = oracle.num_threads()
     rng = np.random.default_rng(0)
-
-    def one_step(n_sample):
-        t0 = time.perf_counter()
-        logits = oracle.router_logits(inp["x"], inp["w_router"], inp["bias"])
-        r = oracle.route(logits, w.M, w.kpg)
-        t_route = time.perf_counter() - t0
-        sample = np.sort(rng.choice(w.T, n_sample, replace=False)).astype(np.int32)
-        t0 = time.perf_counter()
-        oracle.combine_tokens(sample, r["idx"], r["gate64"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
-        t_ffn = time.perf_counter() - t0
-        return t_route / w.T + t_ffn / n_sample
-
-    n_sample = max(1, args.ref_tokens)
+    n_sample = args.ref_tokens if args.ref_tokens > 0 else REF_TOKENS_PER_THREAD * cores
     for _ in range(args.warmup):
-        one_step(n_sample)
-    per_tok = [one_step(n_sample) for _ in range(args.steps)]
+        oracle_layer_rate(w, inp, n_sample, rng)
+    per_tok, wall = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        sec, _, _, _ = oracle_layer_rate(w, inp, n_sample, rng)
+        wall.append(time.perf_counter() - t0)
+        per_tok.append(sec)
     sec = statistics.fmean(per_tok)
     value = round(1.0 / sec, 3)
     sample_desc = (f"{w.name}: each step routes all {w.T} tokens and runs the expert FFN + combine of "
-                   f"{n_sample} sampled tokens; per-token cost extrapolated to T={w.T}")
+                   f"{n_sample} sampled tokens on {cores} threads; tokens/s = per-token cost extrapolated "
+                   f"to T={w.T}")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * w.T * 1e3, 2),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.fmean(wall) * 1e3, 2),
+        "extrapolated_layer_ms": round(sec * w.T * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "M": w.M,
-                                                 "k_per_group": w.kpg, "I": w.I, "seed": DEFAULT_SEED},
+        "data": "synthetic (seeded)", "config": workload_config(w, ws_n),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": sample_desc},
+                         "cpu_model": cpu_model(), "sample": sample_desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
 
 # --------------------------------------------------------------------------------------------
 # DRAM traffic of the grouped GEMM from an ncu capture (profiles/ncu_traffic.json)
@@ -743,10 +925,14 @@ def main():
                     help="replays of the step captured as a CUDA graph (decode: 3x; 0: skip)")
     ap.add_argument("--study-batches", type=int, default=1000, help="Monte-Carlo study batches (0: skip)")
     ap.add_argument("--pangu-steps", type=int, default=30, help="steps at Pangu Pro dims, K'=1 (0: skip)")
+    ap.add_argument("--stress-steps", type=int, default=50, help="steps of the N=256 stress layer (0: skip)")
+    ap.add_argument("--routing-steps", type=int, default=200, help="steps of the routing workload (0: skip)")
+    ap.add_argument("--tiny-steps", type=int, default=200, help="steps of the tiny fp32 layer (0: skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle FFN work")
-    ap.add_argument("--ref-tokens", type=int, default=8, help="FFN tokens per reference-arm step")
+    ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle FFN work")
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="FFN tokens per reference-arm step (0: 4 per oracle thread)")
     ap.add_argument("--record-traffic", metavar="CSV", help="write profiles/ncu_traffic.json from an ncu csv")
     ap.add_argument("--traffic-command", default="", help="the ncu command that made the csv")
     args = ap.parse_args()

@@ -23,8 +23,8 @@ def test_prefill_roofline_is_flops_over_the_launch_time():
     flop = 4.0 * 131072 * 4096 * 1408
     assert rl["bound"] == "tensor" and rl["algorithmic_per_launch"]["flop"] == flop
     assert abs(rl["achieved"] - flop / 2.5e-3 / 1e12) < 0.01
-    assert rl["frac"] == round(rl["achieved"] / 1362.7, 4)
-    assert rl["frac_of_burst"] == round(rl["achieved"] / 1793.3, 4)
+    assert rl["peak"] == 1793.3 and rl["frac"] == round(rl["achieved"] / 1793.3, 4)   # burst is the denominator
+    assert rl["frac_sustained"] == round(rl["achieved"] / 1362.7, 4)
     assert rl["launch_ms"] == 2.5
 
 
@@ -47,8 +47,34 @@ def test_layer_roofline_and_job_throughput():
     counts[:51] = 1
     lr = bench.layer_roofline(w, counts, 0.3, PK)
     assert lr["touched_experts"] == 51
-    assert abs(lr["weight_gbs"] - 51 * 3 * 1408 * 4096 * 2 / 0.3e-3 / 1e9) < 0.1
+    wbytes = 51 * 3 * 1408 * 4096 * 2
+    assert abs(lr["weight_gbs"] - wbytes / 0.3e-3 / 1e9) < 0.1
+    # decode: the HBM time of the touched weights is the roofline
+    assert lr["roofline_ms"] == round(wbytes / 6479.9e9 * 1e3, 4)
     assert bench.job_tokens_per_s(8192, 4, 4.0) == 8192 * 4 / 4e-3
+
+
+def test_stress_layer_roofline_takes_the_larger_of_tensor_and_hbm_time():
+    """The stress layer (T=4096, d=7680, N=256, K=8, I=2048): 6*P*d*I + 2*T*d*N FLOP = 3.108 TFLOP
+    and the weights of the touched experts (3*d*I bf16 values each); the roofline time is the
+    larger of the two times at the measured peaks."""
+    w = WORKLOADS["stress_n256"]
+    counts = np.zeros(w.N, dtype=np.int32)
+    counts[:89] = 1
+    lr = bench.layer_roofline(w, counts, 3.0, PK)
+    flop = 6.0 * 32768 * 7680 * 2048 + 2.0 * 4096 * 7680 * 256
+    wbytes = 89 * 3 * 7680 * 2048 * 2
+    assert lr["flop"] == flop and lr["weight_bytes"] == wbytes and wbytes == 8_399_093_760
+    t_roof = max(flop / 1793.3e12, wbytes / 6479.9e9)
+    assert lr["roofline_ms"] == round(t_roof * 1e3, 4) and lr["roofline_frac"] == round(t_roof / 3e-3, 4)
+    assert lr["tc_frac"] == round(flop / 3e-3 / 1e12 / 1793.3, 4)
+
+
+def test_both_arms_report_the_same_config():
+    w = WORKLOADS["prefill_t8192"]
+    c = bench.workload_config(w, 1)
+    assert c["workload"] == "prefill_t8192" and (c["T"], c["K"], c["I"]) == (8192, 16, 1408)
+    assert c == bench.workload_config(WORKLOADS["prefill_t8192"], 1)
 
 
 def test_traffic_record_sums_the_stage_kernels(tmp_path, monkeypatch):
