@@ -870,29 +870,46 @@ def run_reference(args):
 # DRAM traffic of the grouped GEMM from an ncu capture (profiles/ncu_traffic.json)
 # --------------------------------------------------------------------------------------------
 
-TRAFFIC_KERNELS = {  # part of the ncu kernel name -> (record key, counts the stage's launches)
-    "ffn_tc_pair_kernel<1>": ("prefill_t8192:gate_up", True),
-    "ffn_tc_kernel<0, 0, 0>": ("prefill_t8192:gate_up", False),  # short-block remainder of gate/up
-    "ffn_tc_pair_kernel<0>": ("prefill_t8192:down", True),
-    "ffn_tc_kernel<1, 0, 0>": ("prefill_t8192:down", False),     # short-block remainder of down
-    "ffn_tc_kernel<2, 32, 1>": ("decode_t32:gate_up", True),
-    "ffn_tc_kernel<3, 32, 0>": ("decode_t32:down", True),
-}
+def traffic_stage(name: str, prev_key):
+    """The record key of one grouped-GEMM launch of an ncu capture of this bench, from its kernel
+    name and the key of the GEMM launch before it (launch order: the prefill layer's CTA-pair
+    gate/up, its small-expert weights-as-M gate/up, the pair down, the small-expert down; then the
+    decode layer's weights-as-M gate/up, gathering its rows, and down).  Returns (key, counts the
+    stage's launches) or None for other kernels."""
+    if "ffn_tc_pair_kernel<1>" in name:
+        return "prefill_t8192:gate_up", True
+    if "ffn_tc_pair_kernel<0>" in name:
+        return "prefill_t8192:down", True
+    if "ffn_tc_kernel<2, 32, 1>" in name:
+        return "decode_t32:gate_up", True
+    if "ffn_tc_kernel<2, 32, 0>" in name:   # small experts of the prefill layer
+        return "prefill_t8192:gate_up", False
+    if "ffn_tc_kernel<3, 32, 0>" in name:   # small experts of the prefill layer, or the decode down
+        return ("decode_t32:down", True) if prev_key == "decode_t32:gate_up" else ("prefill_t8192:down", False)
+    return None
 
 
 def record_traffic(csv_path: str, command: str) -> None:
     """dram__bytes_read.sum + dram__bytes_write.sum per stage of each grouped GEMM in an ncu --csv
-    capture of this bench at full size, stamped with the kernel source hash.  A stage is one launch
-    of its main kernel plus, for the prefill, one launch of the short-block remainder kernel: the
-    stage's bytes are the total over both kernels divided by the main kernel's launches."""
+    capture of this bench at full size, stamped with the kernel source hash.  A prefill stage is
+    one launch of the CTA-pair kernel plus one of the small-expert kernel: the stage's bytes are the
+    total over both divided by the pair kernel's launches."""
     import csv
     total, launches = {}, {}
     with open(csv_path) as f:
         rows = [r for r in csv.reader(f) if len(r) > 10]
     hdr = rows[0]
     ki, ii, mi, vi = (hdr.index(k) for k in ("Kernel Name", "ID", "Metric Name", "Metric Value"))
+    stage_of, prev_key = {}, None
+    for r in rows[1:]:  # one stage per launch id, in launch order
+        if r[ii] in stage_of:
+            continue
+        hit = traffic_stage(r[ki], prev_key)
+        stage_of[r[ii]] = hit
+        if hit is not None:
+            prev_key = hit[0]
     for r in rows[1:]:
-        hit = next((v for k, v in TRAFFIC_KERNELS.items() if k in r[ki]), None)
+        hit = stage_of[r[ii]]
         if hit is None or not r[mi].startswith("dram__bytes_"):
             continue
         key, main_kernel = hit

@@ -110,8 +110,9 @@ const char *moge_status_string(moge_status_t s);
 /* Bytes of scratch needed by every call below for this configuration
  * (0 when cfg is invalid).  One workspace may serve all calls of a layer in
  * stream order (calls on different streams need different workspaces).  The
- * first 4096 bytes (the status page) hold the device status word and
- * self-resetting per-tile counters of the router; they must be zero before
+ * first 4096 bytes (the status page) hold the device status word, the
+ * self-resetting per-tile counters of the router and the tile counters of the
+ * grouped GEMM (each launch returns them to zero); they must be zero before
  * first use (see moge_reset_device_status). */
 size_t moge_workspace_bytes(const moge_config_t *cfg);
 

@@ -89,6 +89,10 @@ constexpr int kPermuteChunk = 256;   // tokens per permutation block
 // sits at byte 0 and the small-batch router's self-resetting counter at kTicketOffset.
 constexpr int kStatusPageBytes = 4096;
 constexpr int kTicketOffset = 256;
+// Tile counters of the CTA-pair grouped GEMM launches (next tile, finished CTAs), one 256-byte
+// slot per GEMM of the layer; each launch returns its pair to zero before it ends.
+constexpr int kSchedGateUpOffset = 512;
+constexpr int kSchedDownOffset = 768;
 constexpr int kRouterTileRows = 128;
 constexpr int kDesignSMs = 148;  // B300 SM count: sizes the router's split of the reduction
 

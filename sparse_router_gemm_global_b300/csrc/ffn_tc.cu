@@ -41,45 +41,39 @@ constexpr int kEpiWarp0 = 4;        // epilogue warps 4..7 (TMEM lane quarter = 
 constexpr int kMaxExperts = 1024;
 constexpr int kSmemBudget = 220 * 1024;
 
-enum Mode { NORMAL_GLU = 0, NORMAL_PLAIN = 1, SWAP_GLU = 2, SWAP_PLAIN = 3 };
+// Weights-as-M modes of the single-CTA kernel (values kept from the kernels' earlier names).
+enum Mode { SWAP_GLU = 2, SWAP_PLAIN = 3 };
 
-constexpr int kPairRows = 256;  // token rows of a CTA-pair tile
+constexpr int kPairRows = 256;         // token rows of a CTA-pair tile
+constexpr int kSmallExpertRows = 128;  // experts with at most this many rows take weights-as-M tiles
+constexpr int kSmallExpertTile = 32;   // tokens per weights-as-M tile of those experts
 
-// Which row blocks of an expert with c rows a launch covers.
-//   kBlocksAll:       ceil(c / tok_block) blocks of tok_block rows.
-//   kBlocksPairMain:  the 256-row pair blocks, except a last block of at most 128 rows.
-//   kBlocksSmallRest: that last block (rows 256*floor(c/256) ..), as one 128-row tile.
-// PairMain + SmallRest cover every row once and keep the MMAs of a short last block from running
-// at 256 rows.
-enum BlockRule { kBlocksAll = 0, kBlocksPairMain = 1, kBlocksSmallRest = 2 };
+// Which experts a single-CTA launch covers, and with how many token blocks of tok_block rows.
+//   kBlocksAll:          every expert (the batch's tile plan chose weights-as-M tiles);
+//   kBlocksSmallExperts: only experts with 1..kSmallExpertRows rows (the CTA-pair launch takes
+//                        the others).
+enum BlockRule { kBlocksAll = 0, kBlocksSmallExperts = 1 };
 
 __device__ __forceinline__ int expert_blocks(int c, int tok_block, int rule) {
-    const int rest = c % kPairRows;
-    if (rule == kBlocksPairMain) return c / kPairRows + (rest > kBM ? 1 : 0);
-    if (rule == kBlocksSmallRest) return (rest > 0 && rest <= kBM) ? 1 : 0;
+    if (rule == kBlocksSmallExperts && c > kSmallExpertRows) return 0;
     return (c + tok_block - 1) / tok_block;
 }
 
-// First row (relative to the expert's offset) and row count of block tb of an expert with c rows.
-__device__ __forceinline__ void block_rows(int c, int tb, int tok_block, int rule, int &first, int &n) {
-    first = rule == kBlocksSmallRest ? (c / kPairRows) * kPairRows : tb * tok_block;
-    n = min(tok_block, c - first);
-}
-
+// Tile geometry of the single-CTA weights-as-M kernel: A = 128 weight rows (two A tiles, W_gate
+// and W_up, for gate/up), B = BNT token rows; 128 output features per tile.
 template <int MODE, int BNT>
 struct Cfg {
-    static constexpr bool swap = (MODE == SWAP_GLU || MODE == SWAP_PLAIN);
-    static constexpr bool glu = (MODE == NORMAL_GLU || MODE == SWAP_GLU);
-    static constexpr int mma_n = swap ? BNT : 256;                      // MMA N (rows of operand B)
-    static constexpr int tok_block = swap ? BNT : kBM;                  // tokens per tile
-    static constexpr int feat_block = (swap || glu) ? 128 : 256;        // output features per tile
-    static constexpr int a_tiles = (swap && glu) ? 2 : 1;               // W_gate + W_up as two A tiles
+    static constexpr bool glu = MODE == SWAP_GLU;
+    static constexpr int mma_n = BNT;                                   // MMA N (rows of operand B)
+    static constexpr int tok_block = BNT;                               // tokens per tile
+    static constexpr int feat_block = 128;                              // output features per tile
+    static constexpr int a_tiles = glu ? 2 : 1;                         // W_gate + W_up as two A tiles
     static constexpr int a_bytes = kBM * 128;                           // one 128-row A tile
     static constexpr int b_bytes = mma_n * 128;
     static constexpr int stage_bytes = a_tiles * a_bytes + b_bytes;
     static constexpr int stages_raw = kSmemBudget / stage_bytes;
     static constexpr int stages = stages_raw > 12 ? 12 : stages_raw;
-    static constexpr int acc_cols = swap ? (glu ? 2 * BNT : BNT) : 256;  // fp32 columns per accumulator
+    static constexpr int acc_cols = glu ? 2 * BNT : BNT;                // fp32 columns per accumulator
     static constexpr int tmem_cols = (2 * acc_cols <= 32) ? 32 : (2 * acc_cols <= 64) ? 64
                                    : (2 * acc_cols <= 128) ? 128 : (2 * acc_cols <= 256) ? 256 : 512;
     static constexpr uint32_t idesc = idesc_bf16_f32(kBM, mma_n);
@@ -98,11 +92,14 @@ struct Params {
     const int32_t *row_token;  // [P] token of each permuted row (gathering launches only)
     int rule;                  // BlockRule of the tile list
     int rows;                  // rows of the row buffers (act / out): segments are clamped to them
+    uint32_t *sched;           // CTA-pair launches: {next tile, finished CTAs}, zero between launches
 };
 
-// prefix[e] = sum over e' < e of the row blocks of expert e' (BlockRule); all 256 threads, N <= 1024.
-__device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int rows, int tok_block, int rule,
-                             int32_t *prefix, int32_t *warp_sums) {
+// prefix[e] = sum over e' < e of count(c_e'), c_e' = rows of expert e' (its segment clamped to
+// the buffer's rows); all 256 threads, N <= 1024.
+template <typename CountFn>
+__device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int rows, CountFn count, int32_t *prefix,
+                             int32_t *warp_sums, int32_t *seg_begin = nullptr, int32_t *seg_count = nullptr) {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     int v[4];
     int local = 0;
@@ -111,9 +108,13 @@ __device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int row
         const int e = t * 4 + i;
         int b = 0;
         if (e < N) {
-            int begin, count;
-            expert_segment(offsets, e, rows, begin, count);
-            b = expert_blocks(count, tok_block, rule);
+            int begin, c;
+            expert_segment(offsets, e, rows, begin, c);
+            b = count(c);
+            if (seg_begin) {  // segments cached in shared memory for the per-tile lookups
+                seg_begin[e] = begin;
+                seg_count[e] = c;
+            }
         }
         local += b;
         v[i] = local;
@@ -207,7 +208,9 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     }
     pdl_wait();  // the offsets (and the token rows) come from earlier kernels
     pdl_trigger();
-    build_prefix(p.offsets, p.N, p.rows, C::tok_block, p.rule, prefix, warp_sums);  // contains __syncthreads
+    const int rule = p.rule;
+    build_prefix(p.offsets, p.N, p.rows, [rule](int c) { return expert_blocks(c, C::tok_block, rule); }, prefix,
+                 warp_sums);  // contains __syncthreads
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -224,18 +227,15 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
         // come straight from x (map_a has a one-row box): lane i gathers tile rows 4i..4i+3 with
         // one tile::gather4 copy per k-block, through the row -> token map; otherwise lane 0 loads
         // the rows of the already permuted matrix as one tile.
-        constexpr int tile_rows = C::swap ? (BNT > 0 ? BNT : 16) : kBM;
-        const bool gather_lane = GATHER && lane * 4 < tile_rows;
+        const bool gather_lane = GATHER && lane * 4 < BNT;
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
             int e, tb, fb;
             tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
-            int first, nrows;
             int seg0, cnt;
             expert_segment(p.offsets, e, p.rows, seg0, cnt);
-            block_rows(cnt, tb, C::tok_block, p.rule, first, nrows);
-            const int tok0 = seg0 + first;
+            const int tok0 = seg0 + tb * C::tok_block;
             const int f0 = fb * C::feat_block;
             int r4[4] = {0, 0, 0, 0};
             if (gather_lane) {
@@ -257,30 +257,14 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                 const uint32_t sa = smem_base + s * C::stage_bytes;
                 const uint32_t sb = sa + C::a_tiles * C::a_bytes;
                 const int k0 = kb * kBK;
-                if constexpr (!C::swap) {
-                    if constexpr (GATHER) {
-                        if (gather_lane) tma_gather4(sa + lane * 512, &map_a, fb_, k0, r4[0], r4[1], r4[2], r4[3]);
-                    } else {
-                        if (lane == 0) tma_load_2d(sa, &map_a, fb_, k0, tok0);               // token rows
-                    }
-                    if (lane == 0) {
-                        if constexpr (C::glu) {
-                            tma_load_3d(sb, &map_b0, fb_, k0, f0, e);                        // W_gate rows
-                            tma_load_3d(sb + 128 * 128, &map_b1, fb_, k0, f0, e);            // W_up rows
-                        } else {
-                            tma_load_3d(sb, &map_b0, fb_, k0, f0, e);                        // W_down rows
-                        }
-                    }
+                if (lane == 0) {
+                    tma_load_3d(sa, &map_b0, fb_, k0, f0, e);                                // W_gate / W_down
+                    if (C::glu) tma_load_3d(sa + C::a_bytes, &map_b1, fb_, k0, f0, e);      // W_up
+                }
+                if constexpr (GATHER) {
+                    if (gather_lane) tma_gather4(sb + lane * 512, &map_a, fb_, k0, r4[0], r4[1], r4[2], r4[3]);
                 } else {
-                    if (lane == 0) {
-                        tma_load_3d(sa, &map_b0, fb_, k0, f0, e);                            // W_gate / W_down
-                        if (C::glu) tma_load_3d(sa + C::a_bytes, &map_b1, fb_, k0, f0, e);  // W_up
-                    }
-                    if constexpr (GATHER) {
-                        if (gather_lane) tma_gather4(sb + lane * 512, &map_a, fb_, k0, r4[0], r4[1], r4[2], r4[3]);
-                    } else {
-                        if (lane == 0) tma_load_2d(sb, &map_a, fb_, k0, tok0);               // token rows
-                    }
+                    if (lane == 0) tma_load_2d(sb, &map_a, fb_, k0, tok0);                   // token rows
                 }
             }
         }
@@ -312,7 +296,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
                         const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
                         const uint64_t bdesc = smem_desc_sw128(sb + j * 32);
                         mma_bf16(d_tmem, smem_desc_sw128(sa + j * 32), bdesc, C::idesc, accum);
-                        if (C::swap && C::glu)
+                        if (C::glu)
                             mma_bf16(d_tmem + BNT, smem_desc_sw128(sa + C::a_bytes + j * 32), bdesc, C::idesc,
                                      accum);
                     }
@@ -340,57 +324,17 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
             tc_fence_after();
             int e, tb, fb;
             tile_coords(tile, nfb, prefix, p.N, e, tb, fb);
-            int first, ntok;  // ntok: valid token rows of this tile
             int seg0, cnt;
             expert_segment(p.offsets, e, p.rows, seg0, cnt);
-            block_rows(cnt, tb, C::tok_block, p.rule, first, ntok);
-            const int tok0 = seg0 + first;
+            const int tok0 = seg0 + tb * C::tok_block;
+            const int ntok = min(C::tok_block, cnt - tb * C::tok_block);  // valid token rows of this tile
             const int f0 = fb * C::feat_block;
             const uint32_t t_acc = tmem_base + acc * C::acc_cols + lane_addr;
-            if constexpr (!C::swap) {
-                // thread = token row r; columns = output features
-                const int r = q * 32 + lane;
-                const bool row_ok = r < ntok;
-                __nv_bfloat16 *orow = p.out + (int64_t)(tok0 + r) * p.out_dim;
-                constexpr int chunks = C::glu ? 4 : 8;  // 32-column chunks of output
-#pragma unroll 1
-                for (int c = 0; c < chunks; ++c) {
-                    uint32_t va[32];
-                    float o[32];
-                    tmem_ld_x32(t_acc + c * 32, va);
-                    if constexpr (C::glu) {
-                        uint32_t vu[32];
-                        tmem_ld_x32(t_acc + 128 + c * 32, vu);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            o[j] = swiglu_fast(__uint_as_float(va[j]), __uint_as_float(vu[j]));
-                    } else {
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(va[j]);
-                    }
-                    const int col0 = f0 + c * 32;
-                    if (row_ok) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int col = col0 + v * 8;
-                            if (col < p.out_dim) {  // out_dim is a multiple of 8
-                                uint4 pk;
-                                pk.x = pack_bf16x2(o[v * 8 + 0], o[v * 8 + 1]);
-                                pk.y = pack_bf16x2(o[v * 8 + 2], o[v * 8 + 3]);
-                                pk.z = pack_bf16x2(o[v * 8 + 4], o[v * 8 + 5]);
-                                pk.w = pack_bf16x2(o[v * 8 + 6], o[v * 8 + 7]);
-                                *reinterpret_cast<uint4 *>(orow + col) = pk;
-                            }
-                        }
-                    }
-                }
-            } else {
+            {
                 // thread = output feature f; columns = token rows of the tile
                 const int f = f0 + q * 32 + lane;
                 const bool f_ok = f < p.out_dim;
-                constexpr int CH = BNT < 32 ? (BNT > 0 ? BNT : 16) : 32;
+                constexpr int CH = BNT < 32 ? BNT : 32;
 #pragma unroll 1
                 for (int c = 0; c < C::tok_block / CH; ++c) {
                     float o[CH];
@@ -447,21 +391,94 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------------------------
-// Tokens-as-M tiles on CTA pairs (cluster of 2, tcgen05 cta_group::2).
+// CTA-pair grouped GEMM (cluster of 2, tcgen05 cta_group::2): tokens-as-M tiles of the experts
+// that hold more than kSmallExpertRows rows (the others take weights-as-M tiles in a second,
+// single-CTA launch: see launch_ffn_tc).
 //
 // One MMA covers 256 token rows x 256 outputs: each CTA of the pair loads its 128 token rows
-// and half of the 256 weight rows (gate/up: the even CTA W_gate, the odd CTA W_up; down: 128
-// W_down rows each), so a k-block costs each SM 32 KB instead of 48 KB and the ring holds six
-// stages.  The even CTA's thread issues the MMAs; its full barrier counts the bytes of both
-// CTAs' copies (signalled across the pair), its commits arrive on both CTAs' empty and
-// accumulator-full barriers, and both CTAs' epilogue warps arrive on its accumulator-empty
-// barrier.  Each CTA's TMEM holds its own 128 rows x 256 fp32 columns (double buffered).
+// and half of the 256 weight rows (gate/up: the even CTA W_gate, the odd CTA the matching W_up
+// rows, so one N=256 MMA yields both halves of 128 features and the epilogue applies SwiGLU;
+// down: 128 W_down rows each), so a k-block costs each SM 32 KB and the ring holds six stages.
+// The even CTA's thread issues the MMAs; its full barrier counts the bytes of both CTAs' copies
+// (signalled across the pair), its commits arrive on both CTAs' empty and accumulator-full
+// barriers, and both CTAs' epilogue warps arrive on its accumulator-empty barrier.  Each CTA's
+// TMEM holds its own 128 rows x 256 fp32 columns, double buffered.
 // ---------------------------------------------------------------------------------------------
 constexpr int kPairStageBytes = 2 * kBM * 128;   // per CTA: 128 token rows + 128 weight rows
 constexpr int kPairStages = 6;
 constexpr size_t kPairSmem = (size_t)kPairStages * kPairStageBytes + 1024;
 constexpr uint32_t kPairIdesc = idesc_bf16_f32(256, 256);
 constexpr int kPairTmemCols = 512;               // two 256-column accumulators
+
+// 256-row blocks of an expert with c rows in the CTA-pair launch.
+__device__ __forceinline__ int pair_blocks(int c) { return c > kSmallExpertRows ? (int)cdiv(c, kPairRows) : 0; }
+
+struct PairTile {
+    int e;          // expert
+    int row0;       // first row of the block (row of the activation / output buffers)
+    int nrows;      // valid rows of the block
+    int f0;         // first output feature of the tile
+};
+
+// tile -> PairTile from the prefix and the segments cached in shared memory.
+__device__ __forceinline__ PairTile pair_tile(int tile, const int32_t *prefix, const int32_t *seg_begin,
+                                              const int32_t *seg_count, int N, int nfb, int feat) {
+    int lo = 0, hi = N - 1;  // last e with prefix[e] <= tile (that expert has tiles)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int local = tile - prefix[lo], pb = local / nfb;
+    PairTile t;
+    t.e = lo;
+    t.row0 = seg_begin[lo] + pb * kPairRows;
+    t.nrows = min(kPairRows, seg_count[lo] - pb * kPairRows);
+    t.f0 = (local - pb * nfb) * feat;
+    return t;
+}
+
+// Dynamic tile order.  Tiles are taken in list order from a global counter by whichever pair is
+// free: the tiles in flight stay a narrow window of the list (their A rows and weights stay in
+// L2) and the pairs finish together.  One thread of the even CTA (warp 3, otherwise idle) takes
+// the tile ids and hands them through a small ring in shared memory to both CTAs' producers, the
+// MMA thread and both CTAs' epilogue warps, at most kTileSlots tiles ahead of the slowest of
+// them.  The wait for the counter's reply stays off the threads that issue copies and MMAs, and
+// the MMA thread looks nothing up at a tile boundary (a shared-memory lookup there measured 5 %
+// more cycles: the tensor pipe idles while it runs).
+constexpr int kTileSlots = 4;
+constexpr int kTileSlotReaders = 11;  // even CTA: producer, MMA thread, 4 epilogue warps; odd: producer, 4 epilogue warps
+
+// The scheduler thread's loop: publish tile ids in both CTAs' rings until one is past the list.
+__device__ __forceinline__ void schedule_tiles(int total_tiles, int32_t *ring, uint64_t *full, uint64_t *empty,
+                                               uint32_t *sched, volatile int *abort_v, uint32_t *status) {
+    for (uint32_t k = 0;; ++k) {
+        const int slot = (int)(k % kTileSlots);
+        const uint32_t ph = (k / kTileSlots) & 1;
+        if (!wait_bar_cluster(smem_u32(&empty[slot]), ph ^ 1, abort_v, status)) return;
+        const int tile = (int)min(atomicAdd(sched, 1u), 0x7fffffffu);
+        ring[slot] = tile;
+        st_shared_cluster_u32(mapa_shared(smem_u32(&ring[slot]), 1), (uint32_t)tile);
+        mbar_arrive(smem_u32(&full[slot]));                             // this CTA's readers
+        mbar_arrive_cluster(mapa_shared(smem_u32(&full[slot]), 1));     // the odd CTA's readers
+        if (tile >= total_tiles) return;
+    }
+}
+
+// A reader (one thread): the k-th tile id, after which its slot is released on the even CTA's
+// barrier; -1 when a wait gave up.  Readers in the odd CTA acquire at cluster scope (the id was
+// written from the even CTA).
+__device__ __forceinline__ int read_tile(uint32_t k, int32_t *ring, uint64_t *full, uint64_t *empty, bool leader,
+                                         volatile int *abort_v, uint32_t *status) {
+    const int slot = (int)(k % kTileSlots);
+    const uint32_t ph = (k / kTileSlots) & 1;
+    const uint32_t f = smem_u32(&full[slot]);
+    if (!(leader ? wait_bar(f, ph, abort_v, status) : wait_bar_cluster(f, ph, abort_v, status))) return -1;
+    const int tile = *reinterpret_cast<volatile int32_t *>(&ring[slot]);
+    const uint32_t e = smem_u32(&empty[slot]);
+    if (leader) mbar_arrive(e);
+    else mbar_arrive_cluster(mapa_shared(e, 0));
+    return tile;
+}
 
 template <bool GLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -470,8 +487,11 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     extern __shared__ uint8_t smem_raw[];
     __shared__ int32_t prefix[kMaxExperts + 1];
     __shared__ int32_t warp_sums[8];
+    __shared__ int32_t seg_begin[kMaxExperts], seg_count[kMaxExperts];
     __shared__ __align__(8) uint64_t full_bar[kPairStages], empty_bar[kPairStages];
     __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ __align__(8) uint64_t tile_full[kTileSlots], tile_empty[kTileSlots];
+    __shared__ int32_t tile_ring[kTileSlots];
     __shared__ uint32_t tmem_base_slot;
     __shared__ int abort_flag;
 
@@ -490,6 +510,10 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             mbar_init(smem_u32(&tfull_bar[b]), 1);
             mbar_init(smem_u32(&tempty_bar[b]), 8);  // 4 epilogue warps of each CTA
         }
+        for (int i = 0; i < kTileSlots; ++i) {
+            mbar_init(smem_u32(&tile_full[i]), 1);                  // the scheduler thread
+            mbar_init(smem_u32(&tile_empty[i]), kTileSlotReaders);  // (the even CTA's barrier only)
+        }
         mbar_init(smem_u32(&drain_bar), 1);
         abort_flag = 0;
         fence_mbar_init();
@@ -506,17 +530,17 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     }
     pdl_wait();  // the offsets (and the token rows) come from earlier kernels
     pdl_trigger();
-    build_prefix(p.offsets, p.N, p.rows, kPairRows, p.rule, prefix, warp_sums);  // contains __syncthreads
+    constexpr int feat = GLU ? 128 : 256;  // output features of a tile
+    const int nfb = (p.out_dim + feat - 1) / feat;
+    build_prefix(p.offsets, p.N, p.rows, [nfb](int c) { return pair_blocks(c) * nfb; }, prefix, warp_sums,
+                 seg_begin, seg_count);  // contains __syncthreads
     tc_fence_before();
     cluster_sync();  // both CTAs' barriers are initialised and their TMEM allocated
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_slot;
 
-    constexpr int feat_block = GLU ? 128 : 256;
-    const int nfb = (p.out_dim + feat_block - 1) / feat_block;
-    const int total_tiles = prefix[p.N] * nfb;
+    const int total_tiles = prefix[p.N];
     const int kblocks = (p.kdim + kBK - 1) / kBK;
-    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
     volatile int *abort_v = &abort_flag;
 
     if (warp == 0) {
@@ -524,13 +548,12 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = cid; tile < total_tiles && ok; tile += ncl) {
-                int e, pb, fb;
-                tile_coords(tile, nfb, prefix, p.N, e, pb, fb);
-                int seg0, cnt;
-                expert_segment(p.offsets, e, p.rows, seg0, cnt);
-                const int rows0 = seg0 + pb * kPairRows + (int)rank * kBM;
-                const int f0 = fb * feat_block + (GLU ? 0 : (int)rank * kBM);
+            for (uint32_t k = 0; ok; ++k) {
+                const int tile = read_tile(k, tile_ring, tile_full, tile_empty, leader, abort_v, p.status);
+                if (tile < 0 || tile >= total_tiles) break;
+                const PairTile t = pair_tile(tile, prefix, seg_begin, seg_count, p.N, nfb, feat);
+                const int trow = t.row0 + (int)rank * kBM;                 // this CTA's 128 token rows
+                const int wrow = t.f0 + (GLU ? 0 : (int)rank * kBM);       // and its weight rows
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % kPairStages;
                     const uint32_t ph = (it / kPairStages) & 1;
@@ -540,9 +563,9 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     const uint32_t sa = smem_base + s * kPairStageBytes;
                     const uint32_t sb = sa + kBM * 128;
                     const int k0 = kb * kBK;
-                    tma_load_2d_pair(sa, &map_a, full_leader, k0, rows0);                // 128 token rows
-                    if (GLU && !leader) tma_load_3d_pair(sb, &map_b1, full_leader, k0, f0, e);  // W_up
-                    else tma_load_3d_pair(sb, &map_b0, full_leader, k0, f0, e);          // W_gate / W_down
+                    tma_load_2d_pair(sa, &map_a, full_leader, k0, trow);                       // token rows
+                    if (GLU && !leader) tma_load_3d_pair(sb, &map_b1, full_leader, k0, wrow, t.e);  // W_up
+                    else tma_load_3d_pair(sb, &map_b0, full_leader, k0, wrow, t.e);            // W_gate / W_down
                 }
             }
             // drain (even CTA): its full barriers also count the odd CTA's copies
@@ -556,7 +579,9 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         if (lane == 0 && leader) {
             uint32_t it = 0, local = 0;
             bool ok = true;
-            for (int tile = cid; tile < total_tiles && ok; tile += ncl, ++local) {
+            for (uint32_t k = 0; ok; ++k, ++local) {
+                const int tile = read_tile(k, tile_ring, tile_full, tile_empty, true, abort_v, p.status);
+                if (tile < 0 || tile >= total_tiles) break;
                 const int acc = local & 1;
                 const uint32_t use = local >> 1;
                 if (!wait_bar(smem_u32(&tempty_bar[acc]), (use & 1) ^ 1, abort_v, p.status)) break;
@@ -582,26 +607,31 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             drain_wait(smem_u32(&drain_bar), 0, p.status);
         }
         __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------ tile scheduler (one thread, even CTA)
+        if (lane == 0 && leader)
+            schedule_tiles(total_tiles, tile_ring, tile_full, tile_empty, p.sched, abort_v, p.status);
+        __syncwarp();
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------ epilogue (warps 4..7 of each CTA)
         const int q = warp & 3;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         uint32_t local = 0;
-        for (int tile = cid; tile < total_tiles; tile += ncl, ++local) {
+        for (uint32_t k = 0;; ++k, ++local) {
+            int tile = 0;
+            if (lane == 0) tile = read_tile(k, tile_ring, tile_full, tile_empty, leader, abort_v, p.status);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (tile < 0 || tile >= total_tiles) break;
             const int acc = local & 1;
             const uint32_t use = local >> 1;
             bool ok = wait_bar(smem_u32(&tfull_bar[acc]), use & 1, abort_v, p.status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            int e, pb, fb;
-            tile_coords(tile, nfb, prefix, p.N, e, pb, fb);
-            int seg0, cnt;
-            expert_segment(p.offsets, e, p.rows, seg0, cnt);
-            const int r = (int)rank * kBM + q * 32 + lane;       // row inside the 256-row pair tile
-            const bool row_ok = r < cnt - pb * kPairRows;
-            __nv_bfloat16 *orow = p.out + (int64_t)(seg0 + pb * kPairRows + r) * p.out_dim;
-            const int f0 = fb * feat_block;
+            const PairTile t = pair_tile(tile, prefix, seg_begin, seg_count, p.N, nfb, feat);
+            const int r = (int)rank * kBM + q * 32 + lane;       // row inside the 256-row tile
+            const bool row_ok = r < t.nrows;
+            __nv_bfloat16 *orow = p.out + (int64_t)(t.row0 + r) * p.out_dim;
             const uint32_t t_acc = tmem_base + acc * 256 + lane_addr;
             constexpr int chunks = GLU ? 4 : 8;
 #pragma unroll 1
@@ -620,12 +650,12 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(va[j]);
                 }
-                const int col0 = f0 + c * 32;
+                const int col0 = t.f0 + c * 32;
                 if (row_ok) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         const int col = col0 + v * 8;
-                        if (col < p.out_dim) {
+                        if (col < p.out_dim) {  // out_dim is a multiple of 8
                             uint4 pk;
                             pk.x = pack_bf16x2(o[v * 8 + 0], o[v * 8 + 1]);
                             pk.y = pack_bf16x2(o[v * 8 + 2], o[v * 8 + 3]);
@@ -650,6 +680,15 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     cluster_sync();  // the odd CTA's shared memory and TMEM stay live until the even CTA's MMAs end
     tc_fence_after();
     if (warp == 2) tmem_dealloc_pair(tmem_base, kPairTmemCols);
+    // the last CTA to finish returns the tile counters to zero for the next launch (every CTA
+    // has left its loops, so no scheduler takes another tile)
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -731,24 +770,44 @@ bool make_act_map(CUtensorMap *m, const void *act, const int32_t *row_token, int
     return row_token ? make_map_2d(m, act, T, d, 1) : make_map_2d(m, act, P, d, rows);
 }
 
+// Weights-as-M tiles of BNT tokens for every expert (rule kBlocksAll: the batch's plan) or for
+// the small experts only (kBlocksSmallExperts, beside a CTA-pair launch): gate/up + SwiGLU -> h,
+// and down -> y_perm.
+template <int BNT>
+cudaError_t launch_swap_gate_up(const void *act, const int32_t *row_token, const int32_t *offsets, int64_t N,
+                                int64_t P, int64_t T, int64_t d, int64_t I, const CUtensorMap &mg,
+                                const CUtensorMap &mu, void *h, uint32_t *status, int rule, cudaStream_t s) {
+    CUtensorMap mx;
+    if (!make_act_map(&mx, act, row_token, T, P, d, BNT)) return cudaErrorInvalidValue;
+    const int64_t tok_blocks = rule == kBlocksAll ? cdiv(P, BNT) + N : N * cdiv(kSmallExpertRows, BNT);
+    Params p{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token, rule, (int)P, nullptr};
+    return row_token ? launch_mode<SWAP_GLU, BNT, true>(mx, mg, mu, p, tok_blocks * cdiv(I, 128), s)
+                     : launch_mode<SWAP_GLU, BNT, false>(mx, mg, mu, p, tok_blocks * cdiv(I, 128), s);
+}
+
+template <int BNT>
+cudaError_t launch_swap_down(const int32_t *offsets, int64_t N, int64_t P, int64_t d, int64_t I,
+                             const CUtensorMap &mdn, const void *h, void *y_perm, uint32_t *status, int rule,
+                             cudaStream_t s) {
+    CUtensorMap mh;
+    if (!make_map_2d(&mh, h, P, I, BNT)) return cudaErrorInvalidValue;
+    const int64_t tok_blocks = rule == kBlocksAll ? cdiv(P, BNT) + N : N * cdiv(kSmallExpertRows, BNT);
+    Params p{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, rule, (int)P, nullptr};
+    return launch_mode<SWAP_PLAIN, BNT, false>(mh, mdn, mdn, p, tok_blocks * cdiv(d, 128), s);
+}
+
 template <int BNT>
 cudaError_t launch_swap(const void *act, const int32_t *row_token, const int32_t *offsets, int64_t N, int64_t P,
                         int64_t T, int64_t d, int64_t I, const void *wg, const void *wu, const void *wd, void *h,
                         void *y_perm, uint32_t *status, cudaStream_t s) {
-    CUtensorMap mx, mh, mg, mu, mdn;
-    if (!make_act_map(&mx, act, row_token, T, P, d, BNT) || !make_map_2d(&mh, h, P, I, BNT) ||
-        !make_map_3d(&mg, wg, N, I, d, kBM) || !make_map_3d(&mu, wu, N, I, d, kBM) ||
+    CUtensorMap mg, mu, mdn;
+    if (!make_map_3d(&mg, wg, N, I, d, kBM) || !make_map_3d(&mu, wu, N, I, d, kBM) ||
         !make_map_3d(&mdn, wd, N, d, I, kBM))
         return cudaErrorInvalidValue;
-    const int64_t tok_blocks = cdiv(P, BNT) + N;
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, row_token, kBlocksAll, (int)P};
-    cudaError_t err = row_token
-        ? launch_mode<SWAP_GLU, BNT, true>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s)
-        : launch_mode<SWAP_GLU, BNT, false>(mx, mg, mu, p1, tok_blocks * cdiv(I, 128), s);
+    cudaError_t err = launch_swap_gate_up<BNT>(act, row_token, offsets, N, P, T, d, I, mg, mu, h, status, kBlocksAll, s);
     if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
-    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksAll, (int)P};
-    return launch_mode<SWAP_PLAIN, BNT, false>(mh, mdn, mdn, p2, tok_blocks * cdiv(d, 128), s);
+    return launch_swap_down<BNT>(offsets, N, P, d, I, mdn, h, y_perm, status, kBlocksAll, s);
 }
 
 }  // namespace tc
@@ -790,32 +849,33 @@ cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32
         default:
             break;
     }
-    // many tokens: tokens-as-M tiles of 256 rows on CTA pairs, rows read from x_perm
-    if (row_token) return cudaErrorInvalidValue;
+    // Many tokens: the tile is chosen per expert from its row count, on the device.  Experts with
+    // more than kSmallExpertRows rows take CTA-pair tokens-as-M tiles (their last block padded
+    // to 256 rows: it runs while the expert's weights are still in L2); experts with fewer take
+    // 32-token weights-as-M tiles in a single-CTA launch after it (padding a 256-row block for a
+    // few tokens would cost up to 256/c times the expert's MMA work, and the weights-as-M tiles
+    // stream the weights at nearly the HBM rate).  Rows are read from x_perm.
+    if (row_token || !status) return cudaErrorInvalidValue;
     CUtensorMap mx, mh, mg, mu, mdn;
     if (!make_map_2d(&mx, act, P, d, kBM) || !make_map_2d(&mh, h, P, I, kBM) ||
         !make_map_3d(&mg, w_gate, N, I, d, kBM) || !make_map_3d(&mu, w_up, N, I, d, kBM) ||
         !make_map_3d(&mdn, w_down, N, d, I, kBM))
         return cudaErrorInvalidValue;
-    // 256-row pair tiles for every full block and every last block of more than 128 rows, then
-    // single-CTA 128-row tiles for the last blocks of at most 128 rows (no MMA on 128 padding rows)
-    const int64_t pair_blocks = cdiv(P, kPairRows) + N;  // bound of sum_e ceil(count_e / 256)
-    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, nullptr, kBlocksPairMain, (int)P};
+    // bound of the tile count: sum over experts of ceil(count_e / 256) blocks
+    const int64_t pair_blocks = cdiv(P, kPairRows) + N;
+    uint32_t *sched_gu = status + kSchedGateUpOffset / 4, *sched_dn = status + kSchedDownOffset / 4;
+    Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, nullptr, kBlocksAll, (int)P, sched_gu};
     cudaError_t err = launch_pair<true>(mx, mg, mu, p1, pair_blocks * cdiv(I, 128), s);
-    if (err != cudaSuccess) return err;
-    p1.rule = kBlocksSmallRest;
-    err = launch_mode<NORMAL_GLU, 0, false>(mx, mg, mu, p1, N * cdiv(I, 128), s);
+    if (err == cudaSuccess)
+        err = launch_swap_gate_up<kSmallExpertTile>(act, nullptr, offsets, N, P, T, d, I, mg, mu, h, status,
+                                                    kBlocksSmallExperts, s);
     if (err != cudaSuccess) return err;
     mark_stage(MOGE_STAGE_DOWN, s);
-    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksPairMain,
-              (int)P};
+    Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksAll, (int)P,
+              sched_dn};
     err = launch_pair<false>(mh, mdn, mdn, p2, pair_blocks * cdiv(d, 256), s);
     if (err != cudaSuccess) return err;
-    // the single-CTA down tiles load all 256 W_down rows of their feature block in one box
-    CUtensorMap mdn256;
-    if (!make_map_3d(&mdn256, w_down, N, d, I, 2 * kBM)) return cudaErrorInvalidValue;
-    p2.rule = kBlocksSmallRest;
-    return launch_mode<NORMAL_PLAIN, 0, false>(mh, mdn256, mdn256, p2, N * cdiv(d, 256), s);
+    return launch_swap_down<kSmallExpertTile>(offsets, N, P, d, I, mdn, h, y_perm, status, kBlocksSmallExperts, s);
 }
 
 }  // namespace moge

@@ -169,6 +169,25 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
     return v;
 }
 
+// Store a 32-bit value to the shared memory of a CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// mbarrier wait with cluster-scope acquire: the phase was completed by arrivals with
+// release.cluster semantics from another CTA of the cluster, whose prior writes become visible.
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // All threads of both CTAs: release this CTA's prior shared-memory writes, acquire the peer's.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

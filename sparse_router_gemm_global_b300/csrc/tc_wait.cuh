@@ -29,6 +29,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// wait_bar with cluster-scope acquire (a phase completed by another CTA of the cluster).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                 uint32_t *status, uint64_t timeout_ns = kWaitTimeoutNs) {
+    if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+        if ((n & 31) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > timeout_ns || n > (1u << 30)) {
+                *abort_flag = 1;
+                raise_status(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait that ignores the abort flag: used at exit for copies and MMAs already issued.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t *status) {
     const uint64_t t0 = globaltimer();

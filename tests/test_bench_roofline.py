@@ -4,7 +4,7 @@ The algorithmic work per launch is fixed by the layer's definition: the gate/up 
 FLOP (two projections of every (token, expert) row), and at decode it must at least stream the
 gate and up weights of every touched expert (2*I*d bf16 values each) plus its row input (P*d) and
 h output (P*I).  The traffic recorder sums a stage's kernels (the CTA-pair launch and the
-short-block launch) and divides by the stage's launches.
+small-expert launch) and divides by the stage's launches.
 """
 import json
 
@@ -86,11 +86,15 @@ def test_traffic_record_sums_the_stage_kernels(tmp_path, monkeypatch):
         rows.append([str(i), name, "dram__bytes_write.sum", "byte", f"{wr:,}", *"......"])
         rows.append([str(i), name, "gpu__time_duration.sum", "ns", "1", *"......"])
 
-    pair, rest = "void tc::ffn_tc_pair_kernel<1>(CUtensorMap_st, ...)", "void tc::ffn_tc_kernel<0, 0, 0>(...)"
-    for k in range(3):                       # three prefill gate/up stages
+    pair, small = "void tc::ffn_tc_pair_kernel<1>(CUtensorMap_st, ...)", "void tc::ffn_tc_kernel<2, 32, 0>(...)"
+    pair_dn, small_dn = "void tc::ffn_tc_pair_kernel<0>(CUtensorMap_st, ...)", "void tc::ffn_tc_kernel<3, 32, 0>(...)"
+    for k in range(3):                       # three prefill layers: gate/up and down stages
         add(10 * k, pair, 3_000_000_000, 300_000_000)
-        add(10 * k + 1, rest, 800_000_000, 100_000_000)
+        add(10 * k + 1, small, 800_000_000, 100_000_000)
+        add(10 * k + 2, pair_dn, 1_500_000_000, 500_000_000)
+        add(10 * k + 3, small_dn, 200_000_000, 10_000_000)
     add(99, "void tc::ffn_tc_kernel<2, 32, 1>(...)", 1_100_000_000, 80_000_000)
+    add(100, "void tc::ffn_tc_kernel<3, 32, 0>(...)", 550_000_000, 40_000_000)   # decode down: same name
     csv_path = tmp_path / "launches.csv"
     csv_path.write_text("\n".join(",".join(f'"{c}"' for c in r) for r in rows) + "\n")
     out = tmp_path / "ncu_traffic.json"
@@ -99,5 +103,7 @@ def test_traffic_record_sums_the_stage_kernels(tmp_path, monkeypatch):
     rec = json.loads(out.read_text())
     assert rec["prefill_t8192:gate_up"]["launches"] == 3
     assert rec["prefill_t8192:gate_up"]["dram_bytes_per_launch"] == 4_200_000_000
+    assert rec["prefill_t8192:down"]["dram_bytes_per_launch"] == 2_210_000_000
     assert rec["decode_t32:gate_up"]["dram_bytes_per_launch"] == 1_180_000_000
+    assert rec["decode_t32:down"]["launches"] == 1 and rec["decode_t32:down"]["dram_bytes_per_launch"] == 590_000_000
     assert rec["prefill_t8192:gate_up"]["kernel_sha256_16"] == bench.kernel_hash()
