@@ -45,7 +45,7 @@ constexpr int kSmemBudget = 220 * 1024;
 enum Mode { SWAP_GLU = 2, SWAP_PLAIN = 3 };
 
 constexpr int kPairRows = 256;         // token rows of a CTA-pair tile
-constexpr int kSmallExpertRows = 128;  // experts with at most this many rows take weights-as-M tiles
+constexpr int kSmallExpertRows = 64;   // experts with at most this many rows take weights-as-M tiles
 constexpr int kSmallExpertTile = 32;   // tokens per weights-as-M tile of those experts
 
 // Which experts a single-CTA launch covers, and with how many token blocks of tok_block rows.
