@@ -269,3 +269,38 @@ def test_layer_with_half_a_million_rows():
     inp = synth.layer_inputs(w, seed=32)
     got = run_layer(w, upload_layer(inp))
     check_layer_every_expert(w, inp, got)
+
+
+@pytest.mark.parametrize("d,I", [(256, 192), (384, 136)])
+def test_expert_ffn_per_expert_tile_shapes(d, I):
+    """Experts whose row counts sit on both sides of every per-expert switch of the grouped GEMM
+    (the batch holds > 104 rows per expert on average, so the tile shape is chosen per expert on
+    the device): weights-as-M tiles of 32 tokens for experts of at most 64 rows (1, 31, 32, 33,
+    63, 64), CTA-pair tiles above (65, 127, 128, 129, 255, 256, 257, 511, 512, 1000), with a ragged
+    intermediate size and an empty expert; every row against the oracle."""
+    counts = np.array([1, 31, 32, 33, 63, 64, 0, 65, 127, 128, 129, 255, 256, 257, 511, 512, 1000, 0, 7, 5],
+                      dtype=np.int64)
+    N, M, kpg = 20, 4, 1
+    P = int(counts.sum())
+    T = P // (M * kpg)
+    assert T * M * kpg == P and P / N > 104
+    w = WORKLOADS["decode_t32"].with_(T=T, d=d, N=N, M=M, kpg=kpg, I=I)
+    inp = synth.layer_inputs(w, seed=d + I)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    experts = np.repeat(np.arange(N, dtype=np.int32), counts)
+    tokens = np.random.default_rng(d).integers(0, T, size=P).astype(np.int32)
+    c = config(w)
+    ws = moge.alloc_workspace(c)
+    d_inp = upload_layer(inp)
+    y_perm = torch.empty((P, w.d), dtype=torch.bfloat16, device=DEV)
+    moge.moge_expert_ffn(c, dev(inp["x"][tokens]), dev(offsets), d_inp["w_gate"], d_inp["w_up"], d_inp["w_down"],
+                         y_perm, ws)
+    torch.cuda.synchronize()
+    assert moge.moge_query_device_status(ws) == 0
+    got = host(y_perm)
+    rows_ref = oracle.expert_ffn_pairs(tokens, experts, inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"])
+    for e in range(N):  # per expert, so that a failing tile shape is named
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            err = max_rel_err(got[a:b], rows_ref[a:b])
+            assert err <= TOL["bf16"], f"expert {e} ({counts[e]} rows): max rel err {err:.3e}"
