@@ -1,19 +1,22 @@
 // Grouped expert SwiGLU FFN on 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// Two persistent launches per layer (gate/up + SwiGLU -> h, then down -> y_perm), each with
-// one CTA per SM walking a tile list derived on the device from the expert offsets (no host
-// round trip).  Per CTA: warp 0 issues TMA loads into a shared-memory ring, warp 1 issues
-// tcgen05.mma from one thread into a double-buffered TMEM accumulator, warp 2 owns the TMEM
-// allocation, warps 4-7 drain TMEM (tcgen05.ld), apply the epilogue and store bf16.
+// Each GEMM (gate/up + SwiGLU -> h, then down -> y_perm) runs as persistent launches with one CTA
+// per SM walking a tile list derived on the device from the expert offsets (no host round trip).
+// Per CTA: warp 0 issues TMA loads into a shared-memory ring, warp 1 issues tcgen05.mma from one
+// thread into a double-buffered TMEM accumulator, warp 2 owns the TMEM allocation, warps 4-7 drain
+// TMEM (tcgen05.ld), apply the epilogue and store bf16.
 //
 // Tile shapes (M x N x K = rows of operand A x rows of operand B x 64 per k-block):
-//   tokens-as-M (many tokens per expert, prefill):
-//     gate/up: A = 128 permuted token rows, B = 128 W_gate rows stacked on the matching
-//              128 W_up rows (one N=256 MMA); epilogue h = silu(acc[:, :128]) * acc[:, 128:].
-//     down:    A = 128 h rows, B = 256 W_down rows; epilogue y_perm = acc.
-//   weights-as-M ("swap", few tokens per expert, decode): A = 128 weight rows, B = the
-//     expert's (<= 64) token rows, so the weights stream at full MMA height; gate/up issue one
-//     MMA for W_gate and one for W_up into two TMEM column ranges.
+//   tokens-as-M on CTA pairs (cta_group::2), experts with more than kSmallExpertRows rows of a
+//   batch whose experts hold many rows on average:
+//     gate/up: A = 256 permuted token rows, B = 128 W_gate rows (even CTA) and the matching 128
+//              W_up rows (odd CTA); epilogue h = silu(acc[:, :128]) * acc[:, 128:].
+//     down:    A = 256 h rows, B = 256 W_down rows; epilogue y_perm = acc.
+//     Tiles are taken in list order from a counter (one scheduler thread per pair).
+//   weights-as-M ("swap") on single CTAs: A = 128 weight rows, B = the expert's token rows (BNT
+//     per tile), so the weights stream at full MMA height; gate/up issue one MMA for W_gate and
+//     one for W_up into two TMEM column ranges.  Every expert of a batch whose experts hold few
+//     rows on average, or the experts of at most kSmallExpertRows rows beside the pair launch.
 // Rows of a tile never belong to two experts: the tile list is built per expert, rows past
 // the expert's count (or past the tensor) are loaded (other experts' rows or TMA zero fill)
 // but never stored.
