@@ -610,7 +610,7 @@ def oracle_layer_rate(w, inp, n_ffn, rng):
     return t_route / w.T + t_ffn / n, t_route, t_ffn, n
 
 
-REF_TOKENS_PER_THREAD = 4  # oracle FFN tokens per thread in a reference-arm step
+REF_TOKENS_PER_THREAD = 8  # oracle FFN tokens per thread in a reference-arm step
 
 
 def cpu_baseline(w, inp, wd, budget_s=8.0):
@@ -828,7 +828,7 @@ def run_ours(args):
 
 def run_reference(args):
     """The CPU oracle as it stands, on the host cores.  Each step routes all T tokens and runs the
-    expert FFN + combine of a token sample (4 tokens per oracle thread by default, so that every
+    expert FFN + combine of a token sample (8 tokens per oracle thread by default, so that every
     core works, as in the CPU baseline of our arm); `ms_per_step` is the wall time of the step
     actually run, and the per-token cost extrapolated to a whole T-token layer is reported
     separately as `extrapolated_layer_ms`."""
@@ -949,7 +949,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle FFN work")
     ap.add_argument("--ref-tokens", type=int, default=0,
-                    help="FFN tokens per reference-arm step (0: 4 per oracle thread)")
+                    help="FFN tokens per reference-arm step (0: 8 per oracle thread)")
     ap.add_argument("--record-traffic", metavar="CSV", help="write profiles/ncu_traffic.json from an ncu csv")
     ap.add_argument("--traffic-command", default="", help="the ncu command that made the csv")
     args = ap.parse_args()
