@@ -304,3 +304,17 @@ def test_expert_ffn_per_expert_tile_shapes(d, I):
         if b > a:
             err = max_rel_err(got[a:b], rows_ref[a:b])
             assert err <= TOL["bf16"], f"expert {e} ({counts[e]} rows): max rel err {err:.3e}"
+
+
+def test_grouped_gemm_tile_counters_return_to_zero():
+    """The CTA-pair GEMM launches take their tiles from two counters in the workspace's status page
+    (bytes 512 and 768: next tile, finished CTAs); each launch returns them to zero before it ends,
+    so back-to-back layers and CUDA-graph replays start from zero.  Checked after three layers of
+    the per-expert plan on one workspace."""
+    w = WORKLOADS["decode_t32"].with_(T=1500, d=256, I=192)
+    d_inp = upload_layer(synth.layer_inputs(w, seed=77))
+    ws = moge.alloc_workspace(config(w))
+    for _ in range(3):
+        run_layer(w, d_inp, ws=ws)
+        page = host(ws[:1024].view(torch.int32))
+        assert np.all(page[128:132] == 0) and np.all(page[192:196] == 0), page[128:200]
