@@ -307,6 +307,24 @@ def stage_breakdown(layer, steps):
             for s, name in enumerate(moge.STAGE_NAMES)}
 
 
+def step_distribution(layer, steps, min_warm_s):
+    """Median / min / max of single steps, from a separate pass with one event pair around each
+    step, after its own warm-up: after even a second of idle (the clock sampler shutting down) the
+    SM clock is up at its boost value and the first ~100 ms of steps run faster than the layer's
+    power-capped steady state (measured: a 3.43 ms median without this warm-up against 4.17 ms)."""
+    import torch
+    warm_up(layer, 3, min_warm_s)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record()
+        layer.step()
+        b.record()
+    torch.cuda.synchronize()
+    t = sorted(a.elapsed_time(b) for a, b in evs)
+    return {"median": round(statistics.median(t), 5), "min": round(t[0], 5), "max": round(t[-1], 5), "steps": steps}
+
+
 def graph_steps(layer, steps, dist, min_warm_s=0.0):
     """The same step captured once into a CUDA graph and replayed `steps` times: no host work per
     step (no argument checks, tensor-map encoding or launch calls).  Warm-up: at least 3 replays
@@ -688,6 +706,7 @@ def run_ours(args):
         ms, gate_up_ms, launches = timed_steps(prefill, args.steps, args.warmup, dist, clock=clk,
                                                min_warm_s=WARM_S["prefill"])
     clocks = clk.summary()
+    step_dist = step_distribution(prefill, min(max(args.steps, 20), 100), WARM_S["prefill"])
     stages = stage_breakdown(prefill, min(args.steps, 50))
     counts = prefill.aux["counts"].cpu().numpy()
     score = float(prefill.aux["score"][0].item())
@@ -698,6 +717,7 @@ def run_ours(args):
         dec = Layer(wd, d_inp, device)
         dms, dgate_up_ms, dlaunches = timed_steps(dec, args.decode_steps, max(args.warmup, 3), dist,
                                                   min_warm_s=WARM_S["decode"])
+        dstep_dist = step_distribution(dec, min(max(args.decode_steps, 20), 200), WARM_S["decode"])
         dstages = stage_breakdown(dec, min(args.decode_steps, 100))
         dgraph = None
         if args.graph_steps > 0:
@@ -709,6 +729,7 @@ def run_ours(args):
                   "ms_per_step": round(dms, 4), "steps": args.decode_steps,
                   "roofline": gate_up_roofline(wd, dcounts, dgate_up_ms, pk, peak_kind),
                   "layer_roofline": layer_roofline(wd, dcounts, dms, pk),
+                  "step_ms_distribution": dstep_dist,
                   "stage_share_ms": dstages, "cuda_graph": dgraph, "gpu_launches": int(dlaunches)}
 
     # the prefill step captured as a CUDA graph (after the decode timing: its replays are a
@@ -796,6 +817,7 @@ def run_ours(args):
         "config": workload_config(wp, ws_n),
         "roofline": gate_up_roofline(wp, counts, gate_up_ms, pk, peak_kind, sm_mhz=clocks.get("sm_mhz")),
         "layer_roofline": layer_roofline(wp, counts, ms, pk),
+        "step_ms_distribution": step_dist,
         "stage_share_ms": stages,
         "stage_share_note": ("stage durations from a separate pass with events at every stage boundary "
                              "(those events break the launch overlap): shares of the step, not absolute "
