@@ -11,7 +11,8 @@ import torch
 import oracle
 import sparse_router_gemm_global_b300 as moge
 import synth
-from gpu_util import DEV, config, host, max_rel_err, routing_mismatch_ok, torch_dtype, upload_layer
+from gpu_util import (DEV, config, expert_covering_tokens, host, max_rel_err, routing_mismatch_ok, torch_dtype,
+                      upload_layer)
 from synth import WORKLOADS
 
 pytestmark = pytest.mark.gpu
@@ -60,7 +61,11 @@ def test_shared_layer_matches_oracle(T, d, N, M, kpg, I, S, dtype):
     w = WORKLOADS["decode_t32"].with_(name=f"shared_{T}_{d}", T=T, d=d, N=N, M=M, kpg=kpg, I=I, dtype=dtype)
     inp = synth.layer_inputs(w, seed=T + d, n_shared=S)
     got = run_shared(w, upload_layer(inp), S)
-    toks = None if T <= 300 else np.sort(np.random.default_rng(3).choice(T, 40, replace=False))
+    toks = None
+    if T > 300:  # tokens reaching every tile of every routed expert and of every shared expert
+        perm = oracle.permute(got["topk_idx"], w.N)
+        toks, _ = expert_covering_tokens(perm["offsets"], perm["row_token"], w.T)
+        toks = np.union1d(toks, np.arange(0, w.T, 128)).astype(np.int32)
     check_shared(w, inp, got, S, tokens=toks)
 
 
