@@ -576,25 +576,34 @@ def tiny_bench(steps, device):
             "ms_per_step": round(ms, 5), "steps": steps, "l2": "L2-resident (6.3 MB of fp32 weights)"}
 
 
-def stress_bench(steps, warmup, dist, device, pk, ws_n):
+def stress_bench(steps, warmup, dist, device, pk, ws_n, cpu=False):
     """The large-sparse stress layer (T=4096, d=7680, N=256 in 8 groups of 32, K'=1, I=2048; the
     dimensions of the Pangu Ultra MoE page with MoGE routing imposed): one moge_layer_forward per
     step, 24 GB of expert weights resident (larger than L2).  Both roofline fractions: FLOP of the
     grouped GEMMs + router against the bf16 peaks, and the weight bytes of the touched experts
-    against the HBM peak; `roofline_frac` = max(tensor time, HBM time) / step time."""
+    against the HBM peak; `roofline_frac` = max(tensor time, HBM time) / step time.  With `cpu`,
+    also the oracle on this layer (routing of every token + the FFN of 8 tokens per thread)."""
     w = WORKLOADS["stress_n256"]
     inp = synth.layer_inputs(w, seed=DEFAULT_SEED)
     d_inp = upload(inp, device)
-    del inp
     L = Layer(w, d_inp, device)
     ms, _, launches = timed_steps(L, steps, warmup, dist, min_warm_s=WARM_S["prefill"])
     counts = L.aux["counts"].cpu().numpy()
     res = {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "M": w.M, "k_per_group": w.kpg, "K": w.K, "I": w.I,
            "value": round(job_tokens_per_s(w.T, ws_n, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
            "steps": steps, "gpu_launches": int(launches), "rows_per_expert_max": int(counts.max()),
-           "experts_with_at_most_128_rows": int(((counts > 0) & (counts <= 128)).sum()),
+           "experts_with_at_most_64_rows": int(((counts > 0) & (counts <= 64)).sum()),
            "layer_roofline": layer_roofline(w, counts, ms, pk)}
     del L, d_inp
+    if cpu:
+        import oracle
+        sec, t_route, t_ffn, n = oracle_layer_rate(w, inp, REF_TOKENS_PER_THREAD * oracle.num_threads(),
+                                                   np.random.default_rng(0))
+        res["cpu_baseline"] = {"value": round(1.0 / sec, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+                               "kind": "oracle", "route_s": round(t_route, 3), "ffn_s": round(t_ffn, 3),
+                               "sample": f"routing of all {w.T} tokens + FFN and combine of {n} sampled tokens, "
+                                         f"per-token cost extrapolated"}
+    del inp
     return res
 
 
@@ -662,11 +671,22 @@ def cpu_baseline(w, inp, wd, budget_s=8.0):
                            "ffn_tokens": dn, "extrapolated": dn < wd.T}}
     finally:
         oracle.set_num_threads(cores)
+    # the tiny all-fp32 layer in full, and the routing workload in full (scores given: softmax,
+    # group top-K', gates, permutation, imbalance score)
+    wt = WORKLOADS["tiny_fp32"]
+    sec, _, _, _ = oracle_layer_rate(wt, synth.layer_inputs(wt, seed=DEFAULT_SEED), wt.T, rng)
+    res["tiny_fp32"] = {"value": round(1.0 / sec, 1), "tokens": wt.T}
+    wr = WORKLOADS["routing_16k"]
+    logits = synth.route_logits(DEFAULT_SEED, wr.T, wr.N)
+    t0 = time.perf_counter()
+    oracle.route(logits, wr.M, wr.kpg)
+    res["routing_16k"] = {"value": round(wr.T / (time.perf_counter() - t0), 1), "tokens": wr.T, "k_per_group": wr.kpg}
     res["value"] = res["threads_all"]["prefill"]["value"]
     a = res["threads_all"]["prefill"]
     res["sample"] = (f"{w.name}: routing of all {w.T} tokens + expert FFN and combine of {a['ffn_tokens']} sampled "
-                     f"tokens on {cores} threads, per-token cost extrapolated to T={w.T}; {wd.name} in full; "
-                     f"threads_1: the same at one thread (prefill and decode FFN on samples)")
+                     f"tokens on {cores} threads, per-token cost extrapolated to T={w.T}; {wd.name}, tiny_fp32 and "
+                     f"routing_16k in full; threads_1: prefill and decode at one thread (FFN on samples); the "
+                     f"stress layer's figure is under stress.cpu_baseline")
     return res
 
 
@@ -797,7 +817,8 @@ def run_ours(args):
     stress = None
     if args.stress_steps > 0:
         del prefill, d_inp
-        stress = stress_bench(args.stress_steps, max(args.warmup, 3), dist, device, pk, ws_n)
+        stress = stress_bench(args.stress_steps, max(args.warmup, 3), dist, device, pk, ws_n,
+                              cpu=rank == 0 and ws_n == 1 and not args.no_cpu_baseline)
 
     res = {
         "metric": METRIC,
