@@ -71,9 +71,11 @@ __device__ __forceinline__ void expert_segment(const int32_t *offsets, int e, in
 }
 
 // SwiGLU activation silu(a) * u with silu(a) = a / (1 + exp(-a)).
-// swiglu_fast uses the hardware exp2 approximation (bf16 tensor-core path, whose
-// output is rounded to bf16 anyway); swiglu_precise uses expf (all-fp32 path).
-__device__ __forceinline__ float swiglu_fast(float a, float u) { return a / (1.0f + __expf(-a)) * u; }
+// swiglu_fast uses the hardware exp2 approximation and the approximate division (a few fp32
+// ulps; the bf16 tensor-core path rounds its output to bf16 anyway, and an IEEE division here
+// costs the GEMM epilogue several times the instructions); swiglu_precise uses expf and an IEEE
+// division (all-fp32 path).
+__device__ __forceinline__ float swiglu_fast(float a, float u) { return __fdividef(a, 1.0f + __expf(-a)) * u; }
 __device__ __forceinline__ float swiglu_precise(float a, float u) { return a / (1.0f + expf(-a)) * u; }
 
 // ---------------------------------------------------------------------------------------------

@@ -3,14 +3,15 @@
 // Each GEMM (gate/up + SwiGLU -> h, then down -> y_perm) runs as persistent launches with one CTA
 // per SM walking a tile list derived on the device from the expert offsets (no host round trip).
 // Per CTA: warp 0 issues TMA loads into a shared-memory ring, warp 1 issues tcgen05.mma from one
-// thread into a double-buffered TMEM accumulator, warp 2 owns the TMEM allocation, warps 4-7 drain
-// TMEM (tcgen05.ld), apply the epilogue and store bf16.
+// thread into TMEM accumulators, warp 2 owns the TMEM allocation, warps 4-7 (4-11 in the
+// two-region CTA-pair tiles) drain TMEM (tcgen05.ld), apply the epilogue and store bf16.
 //
 // Tile shapes (M x N x K = rows of operand A x rows of operand B x 64 per k-block):
 //   tokens-as-M on CTA pairs (cta_group::2), experts with more than kSmallExpertRows rows of a
 //   batch whose experts hold many rows on average:
-//     gate/up: A = 256 permuted token rows, B = 128 W_gate rows (even CTA) and the matching 128
-//              W_up rows (odd CTA); epilogue h = silu(acc[:, :128]) * acc[:, 128:].
+//     gate/up: A = 256 permuted token rows, two regions of B = 128 W_gate rows (even CTA) and the
+//              matching 128 W_up rows (odd CTA); epilogue h = silu(acc[:, :128]) * acc[:, 128:]
+//              per region, 256 features of h per tile.
 //     down:    A = 256 h rows, B = 256 W_down rows; epilogue y_perm = acc.
 //     Tiles are taken in list order from a counter (one scheduler thread per pair).
 //   weights-as-M ("swap") on single CTAs: A = 128 weight rows, B = the expert's token rows (BNT
@@ -99,7 +100,7 @@ struct Params {
 };
 
 // prefix[e] = sum over e' < e of count(c_e'), c_e' = rows of expert e' (its segment clamped to
-// the buffer's rows); all 256 threads, N <= 1024.
+// the buffer's rows); every thread of the block (256..512 threads, warp_sums[16]), N <= 1024.
 template <typename CountFn>
 __device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int rows, CountFn count, int32_t *prefix,
                              int32_t *warp_sums, int32_t *seg_begin = nullptr, int32_t *seg_count = nullptr) {
@@ -131,13 +132,14 @@ __device__ void build_prefix(const int32_t *__restrict__ offsets, int N, int row
     if (lane == 31) warp_sums[w] = x;
     __syncthreads();
     if (w == 0) {
-        int s = lane < 8 ? warp_sums[lane] : 0;
+        const int nw = (int)(blockDim.x >> 5);
+        int s = lane < nw ? warp_sums[lane] : 0;
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
+        for (int o = 1; o < 16; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, s, o);
             if (lane >= o) s += y;
         }
-        if (lane < 8) warp_sums[lane] = s;
+        if (lane < nw) warp_sums[lane] = s;
     }
     __syncthreads();
     const int excl = x - local + (w > 0 ? warp_sums[w - 1] : 0);
@@ -176,7 +178,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     using C = Cfg<MODE, BNT>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int32_t prefix[kMaxExperts + 1];
-    __shared__ int32_t warp_sums[8];
+    __shared__ int32_t warp_sums[16];
     __shared__ __align__(8) uint64_t full_bar[C::stages], empty_bar[C::stages];
     __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_slot;
@@ -393,25 +395,79 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
     if (warp == 2) tmem_dealloc(tmem_base, C::tmem_cols);
 }
 
+// Stores a warp's 32 rows x 32 bf16 outputs (thread = row, o its 32 values) as 64-byte row
+// segments: each thread packs its row into the warp's 2 KB staging buffer (16-byte units
+// XOR-swizzled by row, so the eight threads of each shared-memory phase hit distinct banks), then
+// each group of four lanes stores one row's 64 contiguous bytes -- a store instruction covers 8
+// rows in whole 32-byte sectors instead of 32 rows in 16-byte pieces.  Rows >= nvalid and columns
+// >= out_dim are not stored (out_dim is a multiple of 8).
+__device__ __forceinline__ void store_rows_staged(const float (&o)[32], uint4 *stage, int lane,
+                                                  __nv_bfloat16 *out, int64_t row0, int nvalid, int col0,
+                                                  int out_dim) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        uint4 pk;
+        pk.x = pack_bf16x2(o[v * 8 + 0], o[v * 8 + 1]);
+        pk.y = pack_bf16x2(o[v * 8 + 2], o[v * 8 + 3]);
+        pk.z = pack_bf16x2(o[v * 8 + 4], o[v * 8 + 5]);
+        pk.w = pack_bf16x2(o[v * 8 + 6], o[v * 8 + 7]);
+        stage[lane * 4 + (v ^ ((lane >> 1) & 3))] = pk;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 8 * i + (lane >> 2), j = lane & 3;
+        const uint4 pk = stage[r * 4 + (j ^ ((r >> 1) & 3))];
+        const int col = col0 + 8 * j;
+        if (r < nvalid && col < out_dim) *reinterpret_cast<uint4 *>(out + (row0 + r) * out_dim + col) = pk;
+    }
+    __syncwarp();  // the buffer is rewritten by the next chunk
+}
+
 // ---------------------------------------------------------------------------------------------
 // CTA-pair grouped GEMM (cluster of 2, tcgen05 cta_group::2): tokens-as-M tiles of the experts
 // that hold more than kSmallExpertRows rows (the others take weights-as-M tiles in a second,
 // single-CTA launch: see launch_ffn_tc).
 //
-// One MMA covers 256 token rows x 256 outputs: each CTA of the pair loads its 128 token rows
-// and half of the 256 weight rows (gate/up: the even CTA W_gate, the odd CTA the matching W_up
-// rows, so one N=256 MMA yields both halves of 128 features and the epilogue applies SwiGLU;
-// down: 128 W_down rows each), so a k-block costs each SM 32 KB and the ring holds six stages.
+// A tile covers 256 token rows x NREG regions of 256 accumulator columns.  A region is one N=256
+// MMA per 16-deep k-step: each CTA of the pair supplies its 128 token rows (A, shared by the
+// regions) and half of the region's 256 weight rows (gate/up: the even CTA W_gate, the odd CTA
+// the matching W_up rows, so a region yields both halves of 128 features and the epilogue
+// applies SwiGLU; down: 128 W_down rows each, 256 outputs).  Per k-block each SM receives 16 KB
+// of token rows and NREG x 16 KB of weight rows.
+//   NREG = 2 (gate/up): 256 features of h per tile, four 48 KB ring stages.  The two regions share
+//     the token rows, so a k-block costs a quarter fewer operand bytes per FLOP than one region,
+//     which sets the pace here (the copies of one-region tiles, timed alone, take nearly as long
+//     as the whole GEMM).  The accumulator fills all 512 TMEM columns, so the MMAs of the next
+//     tile wait for its drain: each region has its own full / empty barrier pair and its own four
+//     epilogue warps (warps 4-7: region 0, warps 8-11: region 1), so both regions drain at once.
+//     The 4096-deep reduction of gate/up keeps that wait to a few per cent of a tile.  A tile
+//     whose second region starts past the last feature skips that region.
+//   NREG = 1 (down): 256 outputs per tile, six 32 KB stages, two 256-column accumulators used in
+//     turn, so the epilogue of a tile overlaps the MMAs of the next (the short reduction of the
+//     down GEMM, d_ff deep, leaves too little MMA time per tile to hide a drain).
 // The even CTA's thread issues the MMAs; its full barrier counts the bytes of both CTAs' copies
 // (signalled across the pair), its commits arrive on both CTAs' empty and accumulator-full
-// barriers, and both CTAs' epilogue warps arrive on its accumulator-empty barrier.  Each CTA's
-// TMEM holds its own 128 rows x 256 fp32 columns, double buffered.
+// barriers, and both CTAs' epilogue warps arrive on its accumulator-empty barriers.  Each CTA's
+// TMEM holds its own 128 rows x 512 fp32 columns.
 // ---------------------------------------------------------------------------------------------
-constexpr int kPairStageBytes = 2 * kBM * 128;   // per CTA: 128 token rows + 128 weight rows
-constexpr int kPairStages = 6;
-constexpr size_t kPairSmem = (size_t)kPairStages * kPairStageBytes + 1024;
+constexpr int kPairBlockBytes = kBM * 128;                 // 128 rows of one k-block (16 KB)
 constexpr uint32_t kPairIdesc = idesc_bf16_f32(256, 256);
-constexpr int kPairTmemCols = 512;               // two 256-column accumulators
+constexpr int kPairTmemCols = 512;
+
+template <bool GLU, int NREG>
+struct PairCfg {
+    static constexpr int region_feat = GLU ? 128 : 256;                 // output features of a region
+    static constexpr int feat = NREG * region_feat;                     // output features of a tile
+    static constexpr int stage_bytes = (1 + NREG) * kPairBlockBytes;    // per CTA: token rows + weights
+    static constexpr int stages = NREG == 1 ? 6 : 4;
+    static constexpr int epi_warps = 4 * NREG;                          // warps 4 .. 3 + epi_warps
+    static constexpr int threads = 32 * (4 + epi_warps);
+    static constexpr size_t smem = (size_t)stages * stage_bytes + epi_warps * 2048 + 1024;  // ring, staging, align
+    // readers of a tile-ring slot: even CTA producer, MMA thread and epilogue warps; odd CTA
+    // producer and epilogue warps
+    static constexpr int slot_readers = 3 + 2 * epi_warps;
+};
 
 // 256-row blocks of an expert with c rows in the CTA-pair launch.
 __device__ __forceinline__ int pair_blocks(int c) { return c > kSmallExpertRows ? (int)cdiv(c, kPairRows) : 0; }
@@ -440,6 +496,13 @@ __device__ __forceinline__ PairTile pair_tile(int tile, const int32_t *prefix, c
     return t;
 }
 
+// Whether a two-region tile's second region holds output features.  Every expert contributes a
+// multiple of nfb tiles, so the feature block is tile % nfb and no lookup is needed: only the
+// last feature block can lack its second region.
+__device__ __forceinline__ bool pair_tile_two_regions(int tile, int nfb, bool last_has_two) {
+    return last_has_two || (tile % nfb) != nfb - 1;
+}
+
 // Dynamic tile order.  Tiles are taken in list order from a global counter by whichever pair is
 // free: the tiles in flight stay a narrow window of the list (their A rows and weights stay in
 // L2) and the pairs finish together.  One thread of the even CTA (warp 3, otherwise idle) takes
@@ -449,7 +512,6 @@ __device__ __forceinline__ PairTile pair_tile(int tile, const int32_t *prefix, c
 // the MMA thread looks nothing up at a tile boundary (a shared-memory lookup there measured 5 %
 // more cycles: the tensor pipe idles while it runs).
 constexpr int kTileSlots = 4;
-constexpr int kTileSlotReaders = 11;  // even CTA: producer, MMA thread, 4 epilogue warps; odd: producer, 4 epilogue warps
 
 // The scheduler thread's loop: publish tile ids in both CTAs' rings until one is past the list.
 __device__ __forceinline__ void schedule_tiles(int total_tiles, int32_t *ring, uint64_t *full, uint64_t *empty,
@@ -483,15 +545,18 @@ __device__ __forceinline__ int read_tile(uint32_t k, int32_t *ring, uint64_t *fu
     return tile;
 }
 
-template <bool GLU>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool GLU, int NREG>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<GLU, NREG>::threads, 1)
 ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                    const __grid_constant__ CUtensorMap map_b1, const Params p) {
+    using C = PairCfg<GLU, NREG>;
+    constexpr int kStages = C::stages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int32_t prefix[kMaxExperts + 1];
-    __shared__ int32_t warp_sums[8];
+    __shared__ int32_t warp_sums[16];
     __shared__ int32_t seg_begin[kMaxExperts], seg_count[kMaxExperts];
-    __shared__ __align__(8) uint64_t full_bar[kPairStages], empty_bar[kPairStages];
+    __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+    // accumulator barriers: NREG = 1, the two buffers used in turn; NREG = 2, the two regions
     __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ __align__(8) uint64_t tile_full[kTileSlots], tile_empty[kTileSlots];
     __shared__ int32_t tile_ring[kTileSlots];
@@ -505,7 +570,7 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     const uint32_t smem_base = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kPairStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
@@ -514,8 +579,8 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             mbar_init(smem_u32(&tempty_bar[b]), 8);  // 4 epilogue warps of each CTA
         }
         for (int i = 0; i < kTileSlots; ++i) {
-            mbar_init(smem_u32(&tile_full[i]), 1);                  // the scheduler thread
-            mbar_init(smem_u32(&tile_empty[i]), kTileSlotReaders);  // (the even CTA's barrier only)
+            mbar_init(smem_u32(&tile_full[i]), 1);                 // the scheduler thread
+            mbar_init(smem_u32(&tile_empty[i]), C::slot_readers);  // (the even CTA's barrier only)
         }
         mbar_init(smem_u32(&drain_bar), 1);
         abort_flag = 0;
@@ -533,8 +598,8 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     }
     pdl_wait();  // the offsets (and the token rows) come from earlier kernels
     pdl_trigger();
-    constexpr int feat = GLU ? 128 : 256;  // output features of a tile
-    const int nfb = (p.out_dim + feat - 1) / feat;
+    const int nfb = (p.out_dim + C::feat - 1) / C::feat;
+    const bool last_has_two = NREG == 1 || (nfb - 1) * C::feat + C::region_feat < p.out_dim;
     build_prefix(p.offsets, p.N, p.rows, [nfb](int c) { return pair_blocks(c) * nfb; }, prefix, warp_sums,
                  seg_begin, seg_count);  // contains __syncthreads
     tc_fence_before();
@@ -554,57 +619,84 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             for (uint32_t k = 0; ok; ++k) {
                 const int tile = read_tile(k, tile_ring, tile_full, tile_empty, leader, abort_v, p.status);
                 if (tile < 0 || tile >= total_tiles) break;
-                const PairTile t = pair_tile(tile, prefix, seg_begin, seg_count, p.N, nfb, feat);
+                const PairTile t = pair_tile(tile, prefix, seg_begin, seg_count, p.N, nfb, C::feat);
+                const int nreg = (NREG == 2 && pair_tile_two_regions(tile, nfb, last_has_two)) ? 2 : 1;
                 const int trow = t.row0 + (int)rank * kBM;                 // this CTA's 128 token rows
                 const int wrow = t.f0 + (GLU ? 0 : (int)rank * kBM);       // and its weight rows
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int s = it % kPairStages;
-                    const uint32_t ph = (it / kPairStages) & 1;
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
                     if (!wait_bar(smem_u32(&empty_bar[s]), ph ^ 1, abort_v, p.status)) { ok = false; break; }
                     const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[s]), 0);
-                    if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * kPairStageBytes);
-                    const uint32_t sa = smem_base + s * kPairStageBytes;
-                    const uint32_t sb = sa + kBM * 128;
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * (1 + nreg) * kPairBlockBytes);
+                    const uint32_t sa = smem_base + s * C::stage_bytes;
                     const int k0 = kb * kBK;
-                    tma_load_2d_pair(sa, &map_a, full_leader, k0, trow);                       // token rows
-                    if (GLU && !leader) tma_load_3d_pair(sb, &map_b1, full_leader, k0, wrow, t.e);  // W_up
-                    else tma_load_3d_pair(sb, &map_b0, full_leader, k0, wrow, t.e);            // W_gate / W_down
+                    tma_load_2d_pair(sa, &map_a, full_leader, k0, trow);                      // token rows
+                    for (int r = 0; r < nreg; ++r) {
+                        const uint32_t sb = sa + (1 + r) * kPairBlockBytes;
+                        const int wr = wrow + r * C::region_feat;
+                        if (GLU && !leader) tma_load_3d_pair(sb, &map_b1, full_leader, k0, wr, t.e);  // W_up
+                        else tma_load_3d_pair(sb, &map_b0, full_leader, k0, wr, t.e);            // W_gate / W_down
+                    }
                 }
             }
             // drain (even CTA): its full barriers also count the odd CTA's copies
             if (leader)
-                for (uint32_t j = (it > (uint32_t)kPairStages ? it - kPairStages : 0); j < it; ++j)
-                    drain_wait(smem_u32(&full_bar[j % kPairStages]), (j / kPairStages) & 1, p.status);
+                for (uint32_t j = (it > (uint32_t)kStages ? it - kStages : 0); j < it; ++j)
+                    drain_wait(smem_u32(&full_bar[j % kStages]), (j / kStages) & 1, p.status);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one thread, even CTA)
+        // Per tile: wait until every accumulator the tile uses has been drained, issue the
+        // k-blocks (each stage freed by a commit once its MMAs complete), then commit the
+        // accumulators.  (Waiting for a drained accumulator only at the tile's first k-block, after
+        // that stage's copies, or committing the accumulators before the last stage, measured
+        // 8-17 % more time.)
         if (lane == 0 && leader) {
-            uint32_t it = 0, local = 0;
+            uint32_t it = 0, n[2] = {0, 0};  // tiles issued so far into region 0 / region 1
             bool ok = true;
-            for (uint32_t k = 0; ok; ++k, ++local) {
+            for (uint32_t k = 0; ok; ++k) {
                 const int tile = read_tile(k, tile_ring, tile_full, tile_empty, true, abort_v, p.status);
                 if (tile < 0 || tile >= total_tiles) break;
-                const int acc = local & 1;
-                const uint32_t use = local >> 1;
-                if (!wait_bar(smem_u32(&tempty_bar[acc]), (use & 1) ^ 1, abort_v, p.status)) break;
+                const int nreg = (NREG == 2 && pair_tile_two_regions(tile, nfb, last_has_two)) ? 2 : 1;
+                // accumulator barrier of region r and its use count: one region, two buffers in
+                // turn; or two regions, one buffer each
+                int b[NREG];
+                uint32_t u[NREG];
+#pragma unroll
+                for (int r = 0; r < NREG; ++r) {
+                    b[r] = NREG == 1 ? (int)(n[0] & 1) : r;
+                    u[r] = NREG == 1 ? n[0] >> 1 : n[r];
+                }
+#pragma unroll
+                for (int r = 0; r < NREG; ++r)
+                    if (r < nreg && !wait_bar(smem_u32(&tempty_bar[b[r]]), (u[r] & 1) ^ 1, abort_v, p.status)) ok = false;
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * 256;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int s = it % kPairStages;
-                    const uint32_t ph = (it / kPairStages) & 1;
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
                     if (!wait_bar(smem_u32(&full_bar[s]), ph, abort_v, p.status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_base + s * kPairStageBytes;
-                    const uint32_t sb = sa + kBM * 128;
+                    const uint32_t sa = smem_base + s * C::stage_bytes;
 #pragma unroll
-                    for (int j = 0; j < kBK / 16; ++j)
-                        mma_bf16_pair(d_tmem, smem_desc_sw128(sa + j * 32), smem_desc_sw128(sb + j * 32), kPairIdesc,
-                                      (kb > 0 || j > 0) ? 1u : 0u);
+                    for (int r = 0; r < NREG; ++r) {
+                        if (r >= nreg) break;
+#pragma unroll
+                        for (int j = 0; j < kBK / 16; ++j)
+                            mma_bf16_pair(tmem_base + b[r] * 256, smem_desc_sw128(sa + j * 32),
+                                          smem_desc_sw128(sa + (1 + r) * kPairBlockBytes + j * 32), kPairIdesc,
+                                          (kb > 0 || j > 0) ? 1u : 0u);
+                    }
                     mma_commit_pair_mc(smem_u32(&empty_bar[s]), 0x3);  // frees the stage in both CTAs
                 }
                 if (!ok) break;
-                mma_commit_pair_mc(smem_u32(&tfull_bar[acc]), 0x3);    // accumulators ready in both CTAs
+#pragma unroll
+                for (int r = 0; r < NREG; ++r)
+                    if (r < nreg) mma_commit_pair_mc(smem_u32(&tfull_bar[b[r]]), 0x3);  // accumulators ready
+                ++n[0];
+                if (nreg == 2) ++n[1];
             }
             mma_commit_pair(smem_u32(&drain_bar));
             drain_wait(smem_u32(&drain_bar), 0, p.status);
@@ -616,26 +708,28 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             schedule_tiles(total_tiles, tile_ring, tile_full, tile_empty, p.sched, abort_v, p.status);
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        // ------------------------------------------------ epilogue (warps 4..7 of each CTA)
-        const int q = warp & 3;
+        // ------------------------------------------------ epilogue (warps 4 .. 3 + epi_warps of each CTA)
+        const int region = (warp - kEpiWarp0) >> 2;
+        const int q = warp & 3;  // TMEM lane quarter
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        uint32_t local = 0;
-        for (uint32_t k = 0;; ++k, ++local) {
+        uint4 *stage = reinterpret_cast<uint4 *>(smem + kStages * C::stage_bytes) + (warp - kEpiWarp0) * 128;
+        uint32_t n = 0;  // tiles this warp has drained
+        for (uint32_t k = 0;; ++k) {
             int tile = 0;
             if (lane == 0) tile = read_tile(k, tile_ring, tile_full, tile_empty, leader, abort_v, p.status);
             tile = __shfl_sync(0xffffffffu, tile, 0);
             if (tile < 0 || tile >= total_tiles) break;
-            const int acc = local & 1;
-            const uint32_t use = local >> 1;
-            bool ok = wait_bar(smem_u32(&tfull_bar[acc]), use & 1, abort_v, p.status);
+            if (region == 1 && !pair_tile_two_regions(tile, nfb, last_has_two)) continue;
+            const int b = NREG == 1 ? (int)(n & 1) : region;
+            const uint32_t u = NREG == 1 ? n >> 1 : n;
+            bool ok = wait_bar(smem_u32(&tfull_bar[b]), u & 1, abort_v, p.status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const PairTile t = pair_tile(tile, prefix, seg_begin, seg_count, p.N, nfb, feat);
-            const int r = (int)rank * kBM + q * 32 + lane;       // row inside the 256-row tile
-            const bool row_ok = r < t.nrows;
-            __nv_bfloat16 *orow = p.out + (int64_t)(t.row0 + r) * p.out_dim;
-            const uint32_t t_acc = tmem_base + acc * 256 + lane_addr;
+            const PairTile t = pair_tile(tile, prefix, seg_begin, seg_count, p.N, nfb, C::feat);
+            const int warp_row0 = (int)rank * kBM + q * 32;     // the warp's first row inside the 256-row tile
+            const uint32_t t_acc = tmem_base + b * 256 + lane_addr;
+            const int f_region = t.f0 + region * C::region_feat;
             constexpr int chunks = GLU ? 4 : 8;
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
@@ -653,28 +747,16 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(va[j]);
                 }
-                const int col0 = t.f0 + c * 32;
-                if (row_ok) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int col = col0 + v * 8;
-                        if (col < p.out_dim) {  // out_dim is a multiple of 8
-                            uint4 pk;
-                            pk.x = pack_bf16x2(o[v * 8 + 0], o[v * 8 + 1]);
-                            pk.y = pack_bf16x2(o[v * 8 + 2], o[v * 8 + 3]);
-                            pk.z = pack_bf16x2(o[v * 8 + 4], o[v * 8 + 5]);
-                            pk.w = pack_bf16x2(o[v * 8 + 6], o[v * 8 + 7]);
-                            *reinterpret_cast<uint4 *>(orow + col) = pk;
-                        }
-                    }
-                }
+                store_rows_staged(o, stage, lane, p.out, (int64_t)t.row0 + warp_row0, t.nrows - warp_row0,
+                                  f_region + c * 32, p.out_dim);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if (leader) mbar_arrive(smem_u32(&tempty_bar[acc]));
-                else mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+                if (leader) mbar_arrive(smem_u32(&tempty_bar[b]));
+                else mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[b]), 0));
             }
+            ++n;
         }
     }
 
@@ -753,15 +835,16 @@ cudaError_t launch_mode(const CUtensorMap &ma, const CUtensorMap &mb0, const CUt
     return err;
 }
 
-template <bool GLU>
+template <bool GLU, int NREG>
 cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1, const Params &p,
                         int64_t pair_tile_bound, cudaStream_t s) {
-    auto kern = ffn_tc_pair_kernel<GLU>;
-    cudaError_t err = set_max_smem(kern, (int)kPairSmem);
+    using C = PairCfg<GLU, NREG>;
+    auto kern = ffn_tc_pair_kernel<GLU, NREG>;
+    cudaError_t err = set_max_smem(kern, (int)C::smem);
     if (err != cudaSuccess) return err;
     const int grid = (int)std::min<int64_t>(2 * pair_tile_bound, (int64_t)(sm_count() & ~1));  // whole pairs
     if (grid <= 0) return cudaSuccess;
-    err = launch_pdl(kern, dim3(grid), dim3(kThreads), kPairSmem, s, ma, mb0, mb1, p);
+    err = launch_pdl(kern, dim3(grid), dim3(C::threads), C::smem, s, ma, mb0, mb1, p);
     count_launches(1);
     return err;
 }
@@ -868,7 +951,7 @@ cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32
     const int64_t pair_blocks = cdiv(P, kPairRows) + N;
     uint32_t *sched_gu = status + kSchedGateUpOffset / 4, *sched_dn = status + kSchedDownOffset / 4;
     Params p1{offsets, (int)N, (int)d, (int)I, (__nv_bfloat16 *)h, status, nullptr, kBlocksAll, (int)P, sched_gu};
-    cudaError_t err = launch_pair<true>(mx, mg, mu, p1, pair_blocks * cdiv(I, 128), s);
+    cudaError_t err = launch_pair<true, 2>(mx, mg, mu, p1, pair_blocks * cdiv(I, PairCfg<true, 2>::feat), s);
     if (err == cudaSuccess)
         err = launch_swap_gate_up<kSmallExpertTile>(act, nullptr, offsets, N, P, T, d, I, mg, mu, h, status,
                                                     kBlocksSmallExperts, s);
@@ -876,7 +959,7 @@ cudaError_t launch_ffn_tc(const void *act, const int32_t *row_token, const int32
     mark_stage(MOGE_STAGE_DOWN, s);
     Params p2{offsets, (int)N, (int)I, (int)d, (__nv_bfloat16 *)y_perm, status, nullptr, kBlocksAll, (int)P,
               sched_dn};
-    err = launch_pair<false>(mh, mdn, mdn, p2, pair_blocks * cdiv(d, 256), s);
+    err = launch_pair<false, 1>(mh, mdn, mdn, p2, pair_blocks * cdiv(d, PairCfg<false, 1>::feat), s);
     if (err != cudaSuccess) return err;
     return launch_swap_down<kSmallExpertTile>(offsets, N, P, d, I, mdn, h, y_perm, status, kBlocksSmallExperts, s);
 }
