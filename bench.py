@@ -919,9 +919,9 @@ def traffic_stage(name: str, prev_key):
     gate/up, its small-expert weights-as-M gate/up, the pair down, the small-expert down; then the
     decode layer's weights-as-M gate/up, gathering its rows, and down).  Returns (key, counts the
     stage's launches) or None for other kernels."""
-    if "ffn_tc_pair_kernel<1>" in name:
+    if "ffn_tc_pair_kernel<1" in name:     # <GLU = 1, regions>
         return "prefill_t8192:gate_up", True
-    if "ffn_tc_pair_kernel<0>" in name:
+    if "ffn_tc_pair_kernel<0" in name:
         return "prefill_t8192:down", True
     if "ffn_tc_kernel<2, 32, 1>" in name:
         return "decode_t32:gate_up", True

@@ -13,7 +13,7 @@
 //              matching 128 W_up rows (odd CTA); epilogue h = silu(acc[:, :128]) * acc[:, 128:]
 //              per region, 256 features of h per tile.
 //     down:    A = 256 h rows, B = 256 W_down rows; epilogue y_perm = acc.
-//     Tiles are taken in list order from a counter (one scheduler thread per pair).
+//     Tiles are taken in list order from a counter.
 //   weights-as-M ("swap") on single CTAs: A = 128 weight rows, B = the expert's token rows (BNT
 //     per tile), so the weights stream at full MMA height; gate/up issue one MMA for W_gate and
 //     one for W_up into two TMEM column ranges.  Every expert of a batch whose experts hold few
@@ -464,9 +464,11 @@ struct PairCfg {
     static constexpr int epi_warps = 4 * NREG;                          // warps 4 .. 3 + epi_warps
     static constexpr int threads = 32 * (4 + epi_warps);
     static constexpr size_t smem = (size_t)stages * stage_bytes + epi_warps * 2048 + 1024;  // ring, staging, align
-    // readers of a tile-ring slot: even CTA producer, MMA thread and epilogue warps; odd CTA
-    // producer and epilogue warps
-    static constexpr int slot_readers = 3 + 2 * epi_warps;
+    // two-region tiles: the even CTA's producer takes the tile ids just in time (else warp 3 does)
+    static constexpr bool producer_claims = NREG == 2;
+    // readers of a tile-ring slot: even CTA MMA thread, epilogue warps (and producer, unless it
+    // takes the ids); odd CTA producer and epilogue warps
+    static constexpr int slot_readers = 2 + 2 * epi_warps + (producer_claims ? 0 : 1);
 };
 
 // 256-row blocks of an expert with c rows in the CTA-pair launch.
@@ -505,27 +507,44 @@ __device__ __forceinline__ bool pair_tile_two_regions(int tile, int nfb, bool la
 
 // Dynamic tile order.  Tiles are taken in list order from a global counter by whichever pair is
 // free: the tiles in flight stay a narrow window of the list (their A rows and weights stay in
-// L2) and the pairs finish together.  One thread of the even CTA (warp 3, otherwise idle) takes
-// the tile ids and hands them through a small ring in shared memory to both CTAs' producers, the
-// MMA thread and both CTAs' epilogue warps, at most kTileSlots tiles ahead of the slowest of
-// them.  The wait for the counter's reply stays off the threads that issue copies and MMAs, and
-// the MMA thread looks nothing up at a tile boundary (a shared-memory lookup there measured 5 %
-// more cycles: the tensor pipe idles while it runs).
+// L2) and the pairs finish together.  Tile ids reach both CTAs' producers, the MMA thread and both
+// CTAs' epilogue warps through a small ring in shared memory (kTileSlots ids), filled by the even
+// CTA.  The MMA thread looks nothing up at a tile boundary (a shared-memory lookup there measured
+// 5 % more cycles: the tensor pipe idles while it runs).  Who takes the ids:
+//   one-region tiles (all of one length): a scheduler thread (warp 3 of the even CTA) takes each
+//     id as soon as a ring slot frees, a few tiles ahead, so the odd CTA's producer never waits
+//     for one at a tile boundary (taking them just in time made the down GEMM 5-9 % slower);
+//   two-region tiles: the even CTA's producer takes the id of its next tile kClaimAhead k-blocks
+//     before the end of the current tile's copies and publishes it a few k-blocks later.  Ids
+//     taken tiles ahead would make each pair's lead the summed duration of its queued tiles,
+//     which differ with the half-length last feature block; the six tiles that share a row
+//     block's token rows then started tens of microseconds apart and re-read them from DRAM
+//     (gate/up moved 1.5x its algorithmic bytes; 1.02x with ids taken just in time).
 constexpr int kTileSlots = 4;
+constexpr int kClaimAhead = 8;
+constexpr int kPublishAfter = 4;
 
-// The scheduler thread's loop: publish tile ids in both CTAs' rings until one is past the list.
+__device__ __forceinline__ int claim_tile(uint32_t *sched) { return (int)min(atomicAdd(sched, 1u), 0x7fffffffu); }
+
+// Publish the k-th tile id in both CTAs' rings (even CTA); false when a wait gave up.
+__device__ __forceinline__ bool publish_tile(uint32_t k, int tile, int32_t *ring, uint64_t *full, uint64_t *empty,
+                                             volatile int *abort_v, uint32_t *status) {
+    const int slot = (int)(k % kTileSlots);
+    const uint32_t ph = (k / kTileSlots) & 1;
+    if (!wait_bar_cluster(smem_u32(&empty[slot]), ph ^ 1, abort_v, status)) return false;
+    ring[slot] = tile;
+    st_shared_cluster_u32(mapa_shared(smem_u32(&ring[slot]), 1), (uint32_t)tile);
+    mbar_arrive(smem_u32(&full[slot]));                             // this CTA's readers
+    mbar_arrive_cluster(mapa_shared(smem_u32(&full[slot]), 1));     // the odd CTA's readers
+    return true;
+}
+
+// The scheduler thread's loop (one-region tiles): publish ids until one is past the list.
 __device__ __forceinline__ void schedule_tiles(int total_tiles, int32_t *ring, uint64_t *full, uint64_t *empty,
                                                uint32_t *sched, volatile int *abort_v, uint32_t *status) {
     for (uint32_t k = 0;; ++k) {
-        const int slot = (int)(k % kTileSlots);
-        const uint32_t ph = (k / kTileSlots) & 1;
-        if (!wait_bar_cluster(smem_u32(&empty[slot]), ph ^ 1, abort_v, status)) return;
-        const int tile = (int)min(atomicAdd(sched, 1u), 0x7fffffffu);
-        ring[slot] = tile;
-        st_shared_cluster_u32(mapa_shared(smem_u32(&ring[slot]), 1), (uint32_t)tile);
-        mbar_arrive(smem_u32(&full[slot]));                             // this CTA's readers
-        mbar_arrive_cluster(mapa_shared(smem_u32(&full[slot]), 1));     // the odd CTA's readers
-        if (tile >= total_tiles) return;
+        const int tile = claim_tile(sched);
+        if (!publish_tile(k, tile, ring, full, empty, abort_v, status) || tile >= total_tiles) return;
     }
 }
 
@@ -579,7 +598,7 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             mbar_init(smem_u32(&tempty_bar[b]), 8);  // 4 epilogue warps of each CTA
         }
         for (int i = 0; i < kTileSlots; ++i) {
-            mbar_init(smem_u32(&tile_full[i]), 1);                 // the scheduler thread
+            mbar_init(smem_u32(&tile_full[i]), 1);                 // the even CTA's publisher
             mbar_init(smem_u32(&tile_empty[i]), C::slot_readers);  // (the even CTA's barrier only)
         }
         mbar_init(smem_u32(&drain_bar), 1);
@@ -616,14 +635,29 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            int tile = 0;
+            const bool claims = C::producer_claims && leader;  // else the ids come from the ring
+            if (claims) {
+                tile = claim_tile(p.sched);
+                ok = publish_tile(0, tile, tile_ring, tile_full, tile_empty, abort_v, p.status);
+            }
+            const int claim_kb = kblocks > kClaimAhead ? kblocks - kClaimAhead : 0;
+            const int publish_kb = min(claim_kb + kPublishAfter, kblocks - 1);
             for (uint32_t k = 0; ok; ++k) {
-                const int tile = read_tile(k, tile_ring, tile_full, tile_empty, leader, abort_v, p.status);
+                if (!claims) tile = read_tile(k, tile_ring, tile_full, tile_empty, leader, abort_v, p.status);
                 if (tile < 0 || tile >= total_tiles) break;
+                int next = 0;
                 const PairTile t = pair_tile(tile, prefix, seg_begin, seg_count, p.N, nfb, C::feat);
                 const int nreg = (NREG == 2 && pair_tile_two_regions(tile, nfb, last_has_two)) ? 2 : 1;
                 const int trow = t.row0 + (int)rank * kBM;                 // this CTA's 128 token rows
                 const int wrow = t.f0 + (GLU ? 0 : (int)rank * kBM);       // and its weight rows
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    if (claims && kb == claim_kb) next = claim_tile(p.sched);
+                    if (claims && kb == publish_kb &&
+                        !publish_tile(k + 1, next, tile_ring, tile_full, tile_empty, abort_v, p.status)) {
+                        ok = false;
+                        break;
+                    }
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
                     if (!wait_bar(smem_u32(&empty_bar[s]), ph ^ 1, abort_v, p.status)) { ok = false; break; }
@@ -639,6 +673,7 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                         else tma_load_3d_pair(sb, &map_b0, full_leader, k0, wr, t.e);            // W_gate / W_down
                     }
                 }
+                if (claims) tile = next;
             }
             // drain (even CTA): its full barriers also count the odd CTA's copies
             if (leader)
@@ -703,8 +738,8 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         }
         __syncwarp();
     } else if (warp == 3) {
-        // ------------------------------------------------ tile scheduler (one thread, even CTA)
-        if (lane == 0 && leader)
+        // ------------------------------------------------ tile scheduler (one-region tiles: one thread, even CTA)
+        if (!C::producer_claims && lane == 0 && leader)
             schedule_tiles(total_tiles, tile_ring, tile_full, tile_empty, p.sched, abort_v, p.status);
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
@@ -766,7 +801,7 @@ ffn_tc_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     tc_fence_after();
     if (warp == 2) tmem_dealloc_pair(tmem_base, kPairTmemCols);
     // the last CTA to finish returns the tile counters to zero for the next launch (every CTA
-    // has left its loops, so no scheduler takes another tile)
+    // has left its loops, so no tile is taken after this)
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {

@@ -86,8 +86,8 @@ def test_traffic_record_sums_the_stage_kernels(tmp_path, monkeypatch):
         rows.append([str(i), name, "dram__bytes_write.sum", "byte", f"{wr:,}", *"......"])
         rows.append([str(i), name, "gpu__time_duration.sum", "ns", "1", *"......"])
 
-    pair, small = "void tc::ffn_tc_pair_kernel<1>(CUtensorMap_st, ...)", "void tc::ffn_tc_kernel<2, 32, 0>(...)"
-    pair_dn, small_dn = "void tc::ffn_tc_pair_kernel<0>(CUtensorMap_st, ...)", "void tc::ffn_tc_kernel<3, 32, 0>(...)"
+    pair, small = "void tc::ffn_tc_pair_kernel<1, 2>(CUtensorMap_st, ...)", "void tc::ffn_tc_kernel<2, 32, 0>(...)"
+    pair_dn, small_dn = "void tc::ffn_tc_pair_kernel<0, 1>(CUtensorMap_st, ...)", "void tc::ffn_tc_kernel<3, 32, 0>(...)"
     for k in range(3):                       # three prefill layers: gate/up and down stages
         add(10 * k, pair, 3_000_000_000, 300_000_000)
         add(10 * k + 1, small, 800_000_000, 100_000_000)
