@@ -271,13 +271,15 @@ def test_layer_with_half_a_million_rows():
     check_layer_every_expert(w, inp, got)
 
 
-@pytest.mark.parametrize("d,I", [(256, 192), (384, 136)])
+@pytest.mark.parametrize("d,I", [(256, 192), (384, 136), (256, 64), (256, 384)])
 def test_expert_ffn_per_expert_tile_shapes(d, I):
     """Experts whose row counts sit on both sides of every per-expert switch of the grouped GEMM
     (the batch holds > 104 rows per expert on average, so the tile shape is chosen per expert on
     the device): weights-as-M tiles of 32 tokens for experts of at most 64 rows (1, 31, 32, 33,
     63, 64), CTA-pair tiles above (65, 127, 128, 129, 255, 256, 257, 511, 512, 1000), with a ragged
-    intermediate size and an empty expert; every row against the oracle."""
+    intermediate size and an empty expert; every row against the oracle.  The gate/up pair tiles
+    hold two regions of 128 features: a partly filled second region (I = 192, 136), a half-filled
+    first region and no second one (I = 64), and a last feature block of one region (I = 384)."""
     counts = np.array([1, 31, 32, 33, 63, 64, 0, 65, 127, 128, 129, 255, 256, 257, 511, 512, 1000, 0, 7, 5],
                       dtype=np.int64)
     N, M, kpg = 20, 4, 1
