@@ -80,6 +80,8 @@ def test_tiny_fp32_layer():
     (520, 256, 256, 8, 1, 128),    # wide groups (G = 32), many empty experts
     (700, 264, 16, 4, 2, 136),     # hidden size not a multiple of the 64-wide k-block (zero-filled tail)
     (1100, 1024, 64, 8, 2, 256),   # several 256-row tiles per expert, gathered token rows
+    (512, 64, 16, 4, 2, 128),      # CTA-pair tiles with a one-k-block gate/up: the next tile id is taken
+                                   # and published at the first k-block, the producer runs tiles ahead
 ])
 def test_bf16_layer_shapes(T, d, N, M, kpg, I):
     w = WORKLOADS["decode_t32"].with_(name=f"bf16_{T}_{d}_{N}_{M}_{kpg}_{I}", T=T, d=d, N=N, M=M, kpg=kpg, I=I)
